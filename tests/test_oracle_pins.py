@@ -1,0 +1,448 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test fixes one part of the oracle against a library routine, a closed form,
+a brute-force computation in exact (Python integer / Fraction) arithmetic, a value
+printed on the pages, or a hand-derived fixture under tests/golden/.  A plausible
+mistake anywhere in the oracle (a dropped term, a wrong sign or index, a swapped
+operand, a wrong tie rule) fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+D = 256
+
+
+# ----------------------------------------------------------------------------- fp16
+
+def test_fp16_matches_numpy_on_every_exponent(orc):
+    """The oracle's binary16 rounding equals numpy's float32 -> float16 cast (a
+    library routine) for every fp32 exponent, random mantissas and every exact tie."""
+    rng = np.random.default_rng(1)
+    ef = np.arange(256, dtype=np.uint32)
+    pats = []
+    for sign in (0, 1):
+        mant = rng.integers(0, 1 << 23, size=(256, 2048), dtype=np.uint32)
+        pats.append((sign << 31) | (ef[:, None] << 23) | mant)
+        # ties and near-ties for every possible number of dropped bits
+        for drop in range(1, 24):
+            half = np.uint32(1 << (drop - 1))
+            base = rng.integers(0, 1 << 23, size=(256, 8), dtype=np.uint32) & ~np.uint32((1 << drop) - 1)
+            for delta in (0, 1):
+                m = (base | half) + np.uint32(delta) if delta else (base | half)
+                pats.append((sign << 31) | (ef[:, None] << 23) | (m & np.uint32(0x7FFFFF)))
+            pats.append((sign << 31) | (ef[:, None] << 23) | ((base | half) - np.uint32(1)) & np.uint32(0x7FFFFF))
+    bits = np.concatenate([p.reshape(-1) for p in pats]).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = orc.f32_to_f16_array(x)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first {x[bad[0]]!r}: {got[bad[0]]:#x} vs {ref[bad[0]]:#x}"
+
+
+def test_fp16_back_conversion_exact(orc):
+    allh = np.arange(1 << 16, dtype=np.uint16)
+    ref = allh.view(np.float16).astype(np.float32)
+    got = np.array([orc.f16_bits_to_f32(int(h)) for h in allh[::7]], np.float32)
+    fin = np.isfinite(ref[::7])
+    assert np.array_equal(got[fin], ref[::7][fin])
+
+
+# ----------------------------------------------------------------------------- Hadamard
+
+def H_oracle():
+    return np.array([[synth_entry(i, j) for j in range(D)] for i in range(D)])
+
+
+_H = None
+
+
+def synth_entry(i, j):
+    import oracle
+    return oracle.hadamard_entry(i, j)
+
+
+def test_hadamard_is_sylvester_and_orthogonal(orc):
+    """H equals scipy's Sylvester Hadamard matrix and H.H = 256 I exactly."""
+    H = np.array([[orc.hadamard_entry(i, j) for j in range(D)] for i in range(D)], dtype=np.int64)
+    assert np.array_equal(H, scipy.linalg.hadamard(D).astype(np.int64))
+    assert np.array_equal(H @ H, 256 * np.eye(D, dtype=np.int64))
+
+
+def test_rotate_unit_vectors(orc):
+    """rotate(e_k) = H[:, k] / 16 (column k), e.g. e_0 -> all 1/16."""
+    Hs = scipy.linalg.hadamard(D)
+    for k in (0, 1, 37, 128, 255):
+        e = np.zeros(D, np.float32)
+        e[k] = 1.0
+        assert np.array_equal(orc.rotate(e), (Hs[:, k] / 16.0).astype(np.float32))
+
+
+def _round_to_f32(v: Fraction) -> np.float32:
+    """Correct rounding of an exact rational to fp32 (nearest, ties to even), by
+    brute force over the three fp32 neighbours of float32(float(v))."""
+    if v == 0:
+        return np.float32(0.0)
+    c = np.float32(float(v))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    best = None
+    for cand in cands:
+        if not np.isfinite(cand):
+            continue
+        err = abs(Fraction(float(cand)) - v)
+        key = (err, int(np.float32(cand).view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return np.float32(best[1])
+
+
+def _exact_rotation(x: np.ndarray) -> np.ndarray:
+    Hs = scipy.linalg.hadamard(D).astype(np.int64)
+    xs = [Fraction(float(t)) for t in x]
+    return np.array([_round_to_f32(sum((xs[j] if Hs[i, j] > 0 else -xs[j]) for j in range(D)) / 16)
+                     for i in range(D)], np.float32)
+
+
+@pytest.mark.parametrize("case", ["normal", "wide", "subnormal", "cancel"])
+def test_rotate_equals_exact_rational_rounding(orc, case):
+    """The oracle's multi-limb rotation equals exact rational arithmetic followed by
+    one correct fp32 rounding, including extreme exponent spreads."""
+    rng = np.random.default_rng({"normal": 2, "wide": 3, "subnormal": 4, "cancel": 5}[case])
+    if case == "normal":
+        x = rng.standard_normal(D).astype(np.float32)
+    elif case == "wide":
+        x = (rng.standard_normal(D) * 10.0 ** rng.integers(-30, 30, D)).astype(np.float32)
+    elif case == "subnormal":
+        x = (rng.standard_normal(D) * 1e-39).astype(np.float32)   # mostly subnormal fp32
+        x[:4] = [1e-45, -1e-45, 3e-45, 1e-38]
+    else:
+        # near-total cancellation: the sums are tiny, so low-order bits decide
+        x = np.zeros(D, np.float32)
+        x[0], x[1] = 1.0, 1.0 + 2.0 ** -23
+        x[2] = 2.0 ** -60
+        x[3] = -(2.0 ** -100)
+    got = orc.rotate(x)
+    ref = _exact_rotation(x)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_rotate_round_trip_and_norm(orc):
+    """For dyadic sparse y, x = (H/16) y is exact in fp32 and rotate(x) = y exactly;
+    the rotation is orthonormal: ||rotate(x)|| = ||x|| up to fp32 rounding."""
+    Hs = scipy.linalg.hadamard(D).astype(np.float64)
+    rng = np.random.default_rng(6)
+    y = np.zeros(D)
+    idx = rng.choice(D, 12, replace=False)
+    y[idx] = rng.integers(-64, 64, 12) / 8.0
+    x = (Hs @ y) / 16.0
+    assert np.array_equal(x.astype(np.float32).astype(np.float64), x)
+    assert np.array_equal(orc.rotate(x.astype(np.float32)).astype(np.float64), y)
+    z = rng.standard_normal(D).astype(np.float32)
+    rz = orc.rotate(z).astype(np.float64)
+    assert abs(np.linalg.norm(rz) - np.linalg.norm(z.astype(np.float64))) < 1e-6 * np.linalg.norm(z)
+    # the rotation is its own inverse up to the two roundings
+    assert np.max(np.abs(orc.rotate(orc.rotate(z)) - z)) < 1e-6
+
+
+# ----------------------------------------------------------------------------- int8
+
+def _read_int8_golden():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "int8_ties.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        parts = line.split()
+        s = float(parts[0])
+        pairs = [(float(a), int(b)) for a, b in (p.split(":") for p in parts[1:])]
+        rows.append((s, pairs))
+    return rows
+
+
+def test_int8_hand_ties(orc):
+    for s, pairs in _read_int8_golden():
+        x = np.zeros(128, np.float32)
+        for i, (n, _) in enumerate(pairs):
+            x[i] = n * s
+        c, got_s = orc.quant_int8(x)
+        assert got_s == s
+        assert [int(t) for t in c[:len(pairs)]] == [code for _, code in pairs]
+
+
+def test_int8_bound_and_extremes(orc):
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        x = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        c, s = orc.quant_int8(x)
+        a = np.max(np.abs(x))
+        assert s == np.float32(a) / np.float32(127.0)
+        err = np.abs(x.astype(np.float64) - c.astype(np.float64) * s)
+        assert np.all(err <= s / 2 * (1 + 2.0 ** -20))
+        assert abs(int(c[np.argmax(np.abs(x))])) == 127
+        assert np.all(np.abs(c.astype(np.int32)) <= 127)
+    c, s = orc.quant_int8(np.zeros(128, np.float32))
+    assert s == 0.0 and not c.any()
+
+
+# ----------------------------------------------------------------------------- Q4_0
+
+def _read_q4_golden():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "q4_ties.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        parts = line.split()
+        blk, d = int(parts[0]), float(parts[1])
+        trip = [(int(a), float(b), int(c)) for a, b, c in (p.split(":") for p in parts[2:])]
+        rows.append((blk, d, trip))
+    return rows
+
+
+def test_q4_hand_ties_through_rotation(orc):
+    """Blocks built in the rotated domain, fed through x = (H/16) y and the oracle's
+    rotation, give the hand-derived codes and scales."""
+    for blk, d, trip in _read_q4_golden():
+        y = np.zeros(32, np.float32)
+        for lane, val, _ in trip:
+            y[lane] = val
+        Hs = scipy.linalg.hadamard(D).astype(np.float64)
+        full = np.zeros(D)
+        full[32 * blk:32 * blk + 32] = y
+        x = ((Hs @ full) / 16.0).astype(np.float32)
+        yr = orc.rotate(x)
+        assert np.array_equal(yr[32 * blk:32 * blk + 32], y)
+        nib, db = orc.quant_q4_block(yr[32 * blk:32 * blk + 32])
+        assert np.float16(d).view(np.uint16) == db
+        codes = np.concatenate([nib & 15, nib >> 4])
+        want = np.full(32, 8)
+        for lane, _, code in trip:
+            want[lane] = code
+        assert np.array_equal(codes, want), (blk, codes, want)
+        # the other blocks are all zero: d = -0 (0 / -8) and every code 8
+        other = (blk + 1) % 8
+        nib0, d0 = orc.quant_q4_block(yr[32 * other:32 * other + 32])
+        assert d0 == 0x8000 and np.all(nib0 == 0x88)
+
+
+def test_q4_error_bounds(orc):
+    """|y - (q-8) d| <= |d|/2 for unclamped codes; a clamped code (y/d >= 7.5, only
+    for elements opposite in sign to m) errs by at most |d| (1 + 2^-10); m -> 0."""
+    rng = np.random.default_rng(8)
+    n_clamped = 0
+    for trial in range(400):
+        y = (rng.standard_normal(32) * 10.0 ** rng.uniform(-2, 2)).astype(np.float32)
+        if trial % 3 == 0:
+            y[rng.integers(32)] = -np.max(np.abs(y)) * rng.uniform(0.94, 1.0)
+        nib, db = orc.quant_q4_block(y)
+        d = float(np.uint16(db).view(np.float16))
+        q = np.concatenate([nib & 15, nib >> 4]).astype(np.int64)
+        err = np.abs(y.astype(np.float64) - (q - 8) * d)
+        clamped = (q == 15) & (y.astype(np.float64) / d >= 7.5)
+        n_clamped += int(clamped.sum())
+        assert np.all(err[~clamped] <= abs(d) / 2 * (1 + 2.0 ** -20))
+        assert np.all(err[clamped] <= abs(d) * (1 + 2.0 ** -10))
+        im = int(np.argmax(np.abs(y)))
+        assert q[im] == 0
+        assert db == np.float16(np.float32(y[im]) / np.float32(-8.0)).view(np.uint16)
+    assert n_clamped > 0
+
+
+# ----------------------------------------------------------------------------- layout
+
+def test_bytes_per_cell(orc):
+    assert 2 * orc.bytes_per_cell_head(orc.FMT_K8V4) == 816
+    assert 2 * orc.bytes_per_cell_head(orc.FMT_INT8) == 1056
+    # 816 = 512 K codes + 16 K scales + 256 V nibbles + 32 V scales
+    assert 2 * (256 + 8 + 128 + 16) == 816
+
+
+def test_memory_figures_printed_on_pages(orc):
+    sizes = {"k8v4": 2 * orc.bytes_per_cell_head(orc.FMT_K8V4), "int8": 2 * orc.bytes_per_cell_head(orc.FMT_INT8)}
+    n = 0
+    for line in open(os.path.join(GOLDEN, "memory_figures.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        cells, layers, fmt, printed, unit, _src = line.split()
+        gib = int(cells) * int(layers) * sizes[fmt] / 2 ** 30
+        decimals = len(printed.split(".")[1])
+        assert round(gib, decimals) == float(printed), (line, gib)
+        n += 1
+    assert n == 6
+    # the 131K-context KV bytes 1.80 GB -> 1.39 GB (same PR, "Measured" table)
+    assert round(1.80 * 816 / 1056, 2) == 1.39
+
+
+def test_page_layout_hand_offsets(orc):
+    """Cell c of a sequence lives in page pt[c // P], slot c % P; within a page of P
+    cells and H heads the four runs are K codes [P][H][256], K scales [P][H][2] f32,
+    V nibbles [P][H][8][16], V scales [P][H][8] f16 (offsets derived by hand)."""
+    P, H = 2, 2
+    cache = orc.Cache(n_pages=3, P=P, H=H)
+    pt = np.array([[2, 0]], np.int32)                     # cells 0,1 -> page 2; 2,3 -> page 0
+    k = np.zeros((1, 1, H, D), np.float32)
+    v = np.zeros((1, 1, H, D), np.float32)
+    k[0, 0, 1, 5] = 127.0                                # head 1, half 0: s = 1, code[5] = 127
+    k[0, 0, 1, 200] = -2.0 * 127                         # head 1, half 1: s = 2, code[200] = -127
+    v[0, 0, 1, :] = 1.0                                  # rotates to 16 e_0 -> block 0: m = 16, d = -2
+    cache.append(pt, np.array([3]), k, v)                # logical cell 3 -> page 0, slot 1
+    page = 0 * P * 816
+    kc = page + (1 * H + 1) * 256
+    ks = page + 512 * P + (1 * H + 1) * 8
+    vq = page + 528 * P + (1 * H + 1) * 128
+    vs = page + 784 * P + (1 * H + 1) * 16
+    b = cache.buf
+    assert b[kc + 5] == 127 and b[kc + 200].view(np.int8) == -127
+    assert np.frombuffer(b[ks:ks + 8].tobytes(), np.float32).tolist() == [1.0, 2.0]
+    assert b[vq] == (0 | (8 << 4)) and np.all(b[vq + 1:vq + 128] == 0x88)
+    dv = np.frombuffer(b[vs:vs + 16].tobytes(), np.uint16)
+    assert dv[0] == np.float16(-2.0).view(np.uint16) and np.all(dv[1:] == 0x8000)
+    # head 0 of the same cell: all-zero input -> codes 0, scales 0, V codes 8, d = -0
+    kc0 = page + (1 * H + 0) * 256
+    assert not b[kc0:kc0 + 256].any()
+    # nothing else was written
+    touched = np.zeros(b.size, bool)
+    for base, n in ((page + (1 * H) * 256, 512), (page + 512 * P + 2 * H * 8 - 16, 16),
+                    (page + 528 * P + (1 * H) * 128, 256), (page + 784 * P + (1 * H) * 16, 32)):
+        touched[base:base + n] = True
+    assert not b[~touched].any()
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _small_cache(orc, fmt, seed=11, n=77, P=8, H=2):
+    rng = np.random.default_rng(seed)
+    n_pages = (n + P - 1) // P
+    pt = rng.permutation(n_pages + 3)[:n_pages].astype(np.int32)[None]
+    k = rng.standard_normal((1, n, H, D)).astype(np.float32)
+    v = rng.standard_normal((1, n, H, D)).astype(np.float32)
+    k[..., 3] *= 20
+    v[..., 7] *= 20
+    cache = orc.Cache(n_pages + 3, P, H, fmt)
+    cache.append(pt, np.array([0]), k, v)
+    return cache, pt, n
+
+
+@pytest.mark.parametrize("fmt", ["k8v4", "int8"])
+def test_attention_matches_torch_sdpa(orc, fmt):
+    """fp64 attention equals torch's scaled_dot_product_attention (float64, CPU)
+    over the dequantised K and the un-rotated dequantised V, for several visible
+    counts and all 16 query heads (GQA 8)."""
+    import torch
+    f = orc.FMT_K8V4 if fmt == "k8v4" else orc.FMT_INT8
+    cache, pt, n = _small_cache(orc, f)
+    kh, vr, vo = cache.dequant(pt, 0, n)
+    Hs = scipy.linalg.hadamard(D).astype(np.float64)
+    vhat = vr.astype(np.float64) @ Hs.T / 16.0 if fmt == "k8v4" else vr.astype(np.float64)
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((16, D)).astype(np.float32)
+    for vis in (1, 2, 40, n):
+        rs, rh, rv = orc.decode_rows(1, 16, [vis])
+        got = cache.attention(pt, rs, rh, rv, q)
+        for h in range(16):
+            g = h // 8
+            Q = torch.tensor(q[h], dtype=torch.float64)[None, None, None]
+            K = torch.tensor(kh[:vis, g].astype(np.float64))[None, None]
+            V = torch.tensor(vhat[:vis, g])[None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=1.0 / 16.0)[0, 0, 0].numpy()
+            assert np.max(np.abs(got[h] - ref)) < 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_attention_closed_forms(orc):
+    """One visible cell returns that cell's V; q = 0 returns the plain mean of the
+    visible cells' V (equal scores)."""
+    cache, pt, n = _small_cache(orc, orc.FMT_K8V4)
+    kh, vr, vo = cache.dequant(pt, 0, n)
+    Hs = scipy.linalg.hadamard(D).astype(np.float64)
+    vhat = vr.astype(np.float64) @ Hs.T / 16.0
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((16, D)).astype(np.float32)
+    rs, rh, rv = orc.decode_rows(1, 16, [1])
+    one = cache.attention(pt, rs, rh, rv, q)
+    for h in range(16):
+        assert np.max(np.abs(one[h] - vhat[0, h // 8])) < 1e-12
+    rs, rh, rv = orc.decode_rows(1, 16, [n])
+    zero = cache.attention(pt, rs, rh, rv, np.zeros((16, D), np.float32))
+    for h in range(16):
+        assert np.max(np.abs(zero[h] - vhat[:n, h // 8].mean(0))) < 1e-12
+    # V after the exact inverse rotation is close to the un-quantised V's scale
+    assert np.all(np.isfinite(vo))
+
+
+def test_attention_page_permutation_invariance(orc):
+    """The same cells written through two different page tables give identical
+    dequantised values and identical attention."""
+    rng = np.random.default_rng(14)
+    n, P, H = 50, 4, 2
+    k = rng.standard_normal((1, n, H, D)).astype(np.float32)
+    v = rng.standard_normal((1, n, H, D)).astype(np.float32)
+    n_pages = (n + P - 1) // P
+    outs = []
+    for seed in (0, 1):
+        pt = np.random.default_rng(seed).permutation(n_pages)[None].astype(np.int32)
+        c = orc.Cache(n_pages, P, H)
+        c.append(pt, np.array([0]), k, v)
+        q = np.random.default_rng(99).standard_normal((16, D)).astype(np.float32)
+        rs, rh, rv = orc.decode_rows(1, 16, [n])
+        outs.append((c.dequant(pt, 0, n), c.attention(pt, rs, rh, rv, q), c.buf.copy()))
+    for a, b in zip(outs[0][0], outs[1][0]):
+        assert np.array_equal(a, b)
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert not np.array_equal(outs[0][2], outs[1][2])        # the bytes did move
+
+
+def test_attention_modes_cross_check(orc):
+    """Verify query i (sees len - 4 + i cells) equals decode at length len - 4 + i;
+    a prefill row t (sees offset + t + 1) equals decode at that length; the
+    rotated-space result brought back with (H/16) equals the default output."""
+    cache, pt, n = _small_cache(orc, orc.FMT_K8V4, n=60)
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal((5, 16, D)).astype(np.float32)
+    steps = np.array([[n - 4 + i for i in range(5)]])
+    rs, rh, rv = orc.multi_query_rows(steps, 16)
+    ver = cache.attention(pt, rs, rh, rv, q.reshape(-1, D)).reshape(5, 16, D)
+    for i in range(5):
+        a, b, c = orc.decode_rows(1, 16, [n - 4 + i])
+        dec = cache.attention(pt, a, b, c, q[i])
+        assert np.array_equal(dec, ver[i])
+    rot = cache.attention(pt, rs, rh, rv, q.reshape(-1, D), rotate_back=False)
+    Hs = scipy.linalg.hadamard(D).astype(np.float64)
+    assert np.max(np.abs(rot @ Hs.T / 16.0 - ver.reshape(-1, D))) < 1e-12
+
+
+def test_negative_control_detects_corruption(orc):
+    """Planted mistake (in the oracle's cache, on the CPU): one flipped V-scale byte
+    changes the attention output well beyond the comparison tolerance."""
+    cache, pt, n = _small_cache(orc, orc.FMT_K8V4, n=33)
+    rng = np.random.default_rng(16)
+    q = rng.standard_normal((16, D)).astype(np.float32)
+    rs, rh, rv = orc.decode_rows(1, 16, [n])
+    good = cache.attention(pt, rs, rh, rv, q)
+    P, H = cache.P, cache.H
+    page = int(pt[0, 1])
+    vs = page * cache.page_bytes + 784 * P + (0 * H + 0) * 16 + 1
+    cache.buf[vs] ^= 0x40
+    bad = cache.attention(pt, rs, rh, rv, q)
+    assert np.max(np.abs(bad - good)) > 1e-3
+
+
+def test_tie_cells_round_trip(orc):
+    """The generator's tie cells quantise to the hand-derived codes."""
+    tk, tv = synth.tie_cells()
+    c, s = orc.quant_int8(tk[0, 0, :128])
+    assert s == 0.0625
+    assert [int(t) for t in c[:11]] == [127, 2, -2, 126, 4, -4, 0, 2, 0, 126, -126]
+    y = orc.rotate(tv[0, 0])
+    nib, db = orc.quant_q4_block(y[:32])
+    codes = np.concatenate([nib & 15, nib >> 4])
+    assert codes[:9].tolist() == [0, 10, 12, 8, 15, 6, 8, 10, 0]

@@ -1,0 +1,181 @@
+/*
+ * k8v4.h -- C ABI of the k8v4 quantized paged KV cache and its fused attention
+ * for one GB300 GPU (sm_103a).
+ *
+ * The cache format is the hybrid "k8v4" KV cache of the pull request
+ * "--kv k8v4: hybrid KV cache -- INT8 K + Hadamard-rotated Q4_0 V (816 B/cell)"
+ * (section "What"): K is stored as symmetric INT8, V is rotated per head by the
+ * orthonormal 256-point Walsh-Hadamard transform and stored as Q4_0, 816 bytes
+ * per cell at 2 KV heads x head_dim 256.  Attention reads the compressed cache in
+ * three modes (section "How": one fused decode/prefill/verify attention over the
+ * hybrid layout; q is not rotated, the output is computed in rotated space and
+ * rotated back).  The block of a page holds three byte runs -- K codes, K
+ * scales, V q4_0 -- as in "kv: --kv k8v4 streams with --kv-resident" (section
+ * "How").
+ *
+ * Conventions for every call:
+ *  - All array arguments are DEVICE pointers owned by the caller (the library
+ *    never allocates; scratch lives in the caller's workspace).  `stream` is a
+ *    cudaStream_t (NULL = legacy default stream).  Calls are asynchronous.
+ *  - Arguments are validated on the host before any launch; a call that fails
+ *    validation launches nothing and returns a negative k8v4_status.
+ *  - Values that live in device memory (positions, lengths, page-table entries)
+ *    are checked by the kernels: an out-of-range page id, position or length is
+ *    skipped (never dereferenced) and recorded in a device status word that
+ *    k8v4_last_device_status() returns.  No kernel traps or spins.
+ *  - The library never calls exit() and never throws across the ABI.
+ *  - Query head h reads KV head h / 8 (GQA group of 8 query heads).
+ *
+ * Page layout (per page of P cells and H KV heads; r = slot * H + head):
+ *   format K8V4 (408 B per cell and head):
+ *     K codes   int8 [P][H][256]        at 0
+ *     K scales  f32  [P][H][2]          at 256*H*P    (one per 128-lane half)
+ *     V nibbles u8   [P][H][8][16]      at 264*H*P    (byte j of a block:
+ *                                                      code j | code j+16 << 4)
+ *     V scales  f16  [P][H][8]          at 392*H*P
+ *   format INT8 (the 1,056 B/cell comparison arm, 528 B per cell and head):
+ *     K codes [P][H][256] at 0, K scales [P][H][2] f32 at 256*H*P,
+ *     V codes [P][H][256] at 264*H*P, V scales [P][H][2] f32 at 520*H*P.
+ *   Cell c of sequence b lives in page page_table[b * max_pages + c / P],
+ *   slot c % P.
+ *
+ * Arithmetic (bit-exact; where the pages leave a step open the plainest
+ * reading is taken and stated here):
+ *   K half (128 lanes): s = absmax / 127 (fp32 division), code =
+ *     clamp(rint_even(x / s), -127, 127); s == 0 -> codes 0.
+ *   V: y = RN_fp32((H_256 x) / 16), Sylvester H, the sum exact; per 32-block:
+ *     m = element of largest |y| (first index on ties), d = fp16_RN(m / -8),
+ *     code = clamp(rint_even(y / d) + 8, 0, 15); d == 0 -> codes 8.
+ *   Attention: out = softmax(sm_scale * q . Khat) . Vhat, Khat = code * s,
+ *     Vhat = (H/16) * ((code - 8) * d); fp32 result.
+ */
+#ifndef K8V4_H
+#define K8V4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Every entry point returns one of these. */
+typedef enum {
+  K8V4_OK = 0,
+  K8V4_EINVAL = -1,  /* a NULL pointer, a bad enum, a size or shape out of range */
+  K8V4_ERANGE = -2,  /* (device) a position, length or page id out of range */
+  K8V4_EALIGN = -3,  /* a pointer not aligned as documented */
+  K8V4_ECUDA = -4,   /* a CUDA runtime call failed (launch, attribute, ...) */
+  K8V4_EDEVICE = -5, /* no sm_103 device, or the library was built for another */
+  K8V4_ENOSPACE = -6 /* the caller's workspace is smaller than required */
+} k8v4_status;
+
+/* Element type of K/V/q inputs. */
+typedef enum { K8V4_F32 = 0, K8V4_BF16 = 1 } k8v4_dtype;
+
+/* Cache format.  3 matches the pages' number for the hybrid format
+ * ("KvFormat gains kKvHybrid = 3"); 1 is the all-INT8 comparison format. */
+typedef enum { K8V4_FORMAT_INT8 = 1, K8V4_FORMAT_K8V4 = 3 } k8v4_format;
+
+/* Descriptor of a caller-owned paged cache (plain data, no ownership). */
+typedef struct {
+  void* pages;        /* device; n_pages * page_size * k8v4_bytes_per_cell() bytes,
+                         256-byte aligned */
+  int64_t n_pages;    /* number of physical pages, >= 1 */
+  int32_t page_size;  /* P, cells per page: a multiple of 16, 16..4096 */
+  int32_t n_kv_heads; /* H, 1..8 */
+  int32_t head_dim;   /* must be 256 */
+  int32_t format;     /* k8v4_format */
+} k8v4_cache;
+
+/* Bytes per cell (all H heads) of a format: 816 for K8V4 at H = 2, 1,056 for
+ * INT8 at H = 2 ("816 B per cell vs int8's 1,056", the k8v4 PR, "What").
+ * Returns 0 for an unknown format or H outside 1..8. */
+size_t k8v4_bytes_per_cell(int32_t format, int32_t n_kv_heads);
+
+/* Human-readable name of a status code (static string). */
+const char* k8v4_status_string(int status);
+
+/* K8V4_OK if the current device is an sm_103 part this library was built for,
+ * else K8V4_EDEVICE. */
+int k8v4_device_check(void);
+
+/* Quantise n_tok new tokens per sequence and write them through the page table
+ * (the append of the k8v4 PR, "How": K to INT8, V rotated then Q4_0; the
+ * per-step decode, verify-window and prompt appends of the streaming PR are all
+ * this call with different n_tok).
+ *   page_table: int32 [n_seqs][max_pages], physical page ids in [0, n_pages).
+ *   pos:        int64 [n_seqs], first logical cell written for sequence b;
+ *               cells pos[b] .. pos[b] + n_tok - 1 are written.
+ *   k, v:       [n_seqs][n_tok][H][256] of `dtype` (K8V4_F32 or K8V4_BF16),
+ *               16-byte aligned, finite values with |x| < 2^100.
+ * Device-side: a cell whose page index reaches max_pages or whose page id is
+ * out of range is skipped and K8V4_ERANGE is recorded.
+ * The exact rotation has a rarely-taken slow path for vectors whose values span
+ * more than 2^55 in magnitude; the result is the same either way. */
+int kv_append_k8v4(const k8v4_cache* cache, const int32_t* page_table, int64_t max_pages, int32_t n_seqs,
+                   const int64_t* pos, int32_t n_tok, const void* k, const void* v, int32_t dtype,
+                   void* stream);
+
+/* Workspace bytes attn_k8v4_decode / attn_k8v4_verify need for a launch with
+ * these host-side bounds (the split-K partial results). */
+size_t attn_k8v4_workspace_bytes(const k8v4_cache* cache, int32_t n_seqs, int32_t n_q_per_seq,
+                                 int32_t max_seq_len);
+
+/* Decode attention: one query (16 heads at H = 2) per sequence over its
+ * seq_lens[b] visible cells (the step form of the PR's mode-3 attention, "Tests").
+ *   q:        [n_seqs][8*H][256] of q_dtype (not rotated), 16-byte aligned.
+ *   seq_lens: int32 [n_seqs] (device), each in [0, max_seq_len].
+ *   max_seq_len: host-side upper bound of seq_lens, <= max_pages * P; sizes the
+ *             split-K grid.  A longer device length is clipped and recorded.
+ *   out:      float [n_seqs][8*H][256], the un-rotated attention output.
+ *   workspace: >= attn_k8v4_workspace_bytes(cache, n_seqs, 1, max_seq_len)
+ *             bytes of device memory, 256-byte aligned.
+ * A row with zero visible cells outputs zeros.  Works on both formats. */
+int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
+                     int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
+                     float sm_scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Verify attention: n_q queries per sequence, query i of sequence b seeing
+ * step_arrays[b][i] cells (the batched form with per-query step arrays, as
+ * verify uses it, the k8v4 PR "Tests"; for a speculative window of 4 drafts + 1
+ * the steps are len-4 .. len).
+ *   q: [n_seqs][n_q][8*H][256]; out: float [n_seqs][n_q][8*H][256];
+ *   step_arrays: int32 [n_seqs][n_q] (device), each in [0, max_seq_len];
+ *   1 <= n_q <= 8. */
+int attn_k8v4_verify(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
+                     int64_t max_pages, const int32_t* step_arrays, int32_t n_seqs, int32_t n_q,
+                     int32_t max_seq_len, float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Chunked-prefill attention for one sequence on the tensor cores (tcgen05):
+ * n_q_tok query tokens, token t seeing step_arrays[t] cells, or, when
+ * step_arrays is NULL, the causal count seq_len - n_q_tok + t + 1 (the chunk
+ * occupies the last n_q_tok cells of seq_len).
+ *   q: bf16 [n_q_tok][8*H][256]; out: float [n_q_tok][8*H][256];
+ *   page_table: int32 [max_pages] for the one sequence; seq_len <= max_pages * P.
+ * K8V4 format only. */
+int attn_k8v4_prefill(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
+                      int64_t max_pages, int32_t seq_len, int32_t n_q_tok, const int32_t* step_arrays,
+                      float sm_scale, float* out, void* stream);
+
+/* Dequantise cells [start, start + n_cells) of one sequence, for checking (the
+ * PR's gather entry points, "Tests": appends and gathers checked bitwise).
+ *   k_out:     float [n_cells][H][256] = code * s
+ *   v_rot_out: float [n_cells][H][256] = (code - 8) * d (rotated space; for the
+ *              INT8 format: code * s, unrotated)
+ *   v_out:     NULL or float [n_cells][H][256] = RN_fp32((H/16) v_rot), the
+ *              exact inverse rotation (INT8 format: a copy of v_rot_out). */
+int kv_dequant_k8v4(const k8v4_cache* cache, const int32_t* page_table, int64_t max_pages, int64_t start,
+                    int64_t n_cells, float* k_out, float* v_rot_out, float* v_out, void* stream);
+
+/* Synchronise `stream`, return the first device-side error recorded since the
+ * last call (K8V4_OK if none) and clear it.  The word is per device and shared
+ * by all streams. */
+int k8v4_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K8V4_H */

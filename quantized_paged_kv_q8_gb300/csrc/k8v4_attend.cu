@@ -1,0 +1,653 @@
+// Split-K flash-decode attention over the k8v4 (or INT8) paged cache, for decode
+// (one query per sequence) and verify (n_q queries per sequence with per-query
+// step arrays): the fused "mode 3" attention of the hybrid-KV pull request
+// ("How": the K loader takes the int8 branch, the V loop the q4 branch, q is not
+// rotated and the output is rotated back; "Tests": step and batched forms with
+// per-query step arrays).
+//
+// GB300 design.  One warp owns one query (the 8 query heads of a KV head) and a
+// stream of 16-cell tiles.  Tiles are staged into shared memory with 16-byte
+// cp.async copies (three stages per tile group), dequantised in registers and
+// fed to warp-level tensor-core MMAs (mma.sync m16n8k16), because at GQA 8 the
+// decode loop needs about 10 FMA per cache byte, more than the fp32 pipes can
+// give at HBM speed:
+//   QK^T: A = K codes (16 cells x 16 dims, int8 -> fp16 exactly), B = q (fp16,
+//         scaled per head by a power of two; an fp32 q is split into two fp16
+//         terms), separate fp32 accumulators for the two 128-lane halves so the
+//         two K scales apply after the MMA.
+//   PV:   A = V codes (16 rotated dims x 16 cells, nibble -> bf16 exactly via
+//         ldmatrix.trans), B = p * d per 32-lane block, split into three bf16
+//         terms (24 significant bits), accumulated in fp32 in rotated space.
+// Online softmax in the log2 domain.  Each CTA writes one partial (m, l, o) per
+// query row; a combine kernel merges the splits and applies the inverse
+// Walsh-Hadamard transform (out = (H/16) o) for the k8v4 format.
+#include <algorithm>
+
+#include "k8v4_common.cuh"
+
+namespace k8v4 {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kStages = 3;
+constexpr int kPStride = 260;   // floats per partial row: o[256], m, l, 2 pad
+constexpr int kPlanes = 3;      // bf16 terms of p * d
+
+template <int FMT>
+struct Stage {
+  static constexpr int kK = 0;                                            // K codes [16][256], swizzled
+  static constexpr int kV = 16 * 256;                                     // V [16][128 or 256], swizzled
+  static constexpr int kVBytes = FMT == K8V4_FORMAT_K8V4 ? 16 * 128 : 16 * 256;
+  static constexpr int kKs = kV + kVBytes;                                // K scales [16][2] f32
+  static constexpr int kVs = kKs + 16 * 8;                                // V scales [16][8] f16 or [16][2] f32
+  static constexpr int kBytes = kVs + (FMT == K8V4_FORMAT_K8V4 ? 16 * 16 : 16 * 8);
+};
+
+struct AttendParams {
+  CacheView C;
+  const void* q;
+  const int32_t* pt;
+  int64_t max_pages;
+  const int32_t* steps;
+  int n_seqs, n_q, n_groups, max_seq_len, cells_per_split, splits;
+  float sm_scale_log2;
+  float* ws;
+  int* status;
+};
+
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ void mma_f16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+__device__ __forceinline__ void ldmatrix_x4_t(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+// two fp32 -> bf16x2 (round to nearest even); `lo` lands in the low half
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// four int8 codes -> two fp16x2 (exact): 0x64XX is 1024 + XX in fp16
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;            // c + 128
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  uint32_t a = prmt(u, 0x64646464u, 0x4140u), b = prmt(u, 0x64646464u, 0x4342u);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+// two nibbles at bits k and k+16 -> bf16x2 of (n - 8), exact: 0x43XX is 128 + XX
+__device__ __forceinline__ uint32_t nib_to_bf16(uint32_t r, int k) {
+  uint32_t t = ((r >> k) & 0x000f000fu) | 0x43004300u;
+  const __nv_bfloat162 bias = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
+  __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t), bias);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// bytes k0 and k1 of r (int8 codes) -> bf16x2 {c_k0, c_k1}, exact
+__device__ __forceinline__ uint32_t i8_to_bf16(uint32_t r, uint32_t s0, uint32_t s1) {
+  const uint32_t u = r ^ 0x80808080u;
+  const float f0 = __uint_as_float(prmt(u, 0x4b000000u, s0)) - 8388736.0f;   // 2^23 + 128
+  const float f1 = __uint_as_float(prmt(u, 0x4b000000u, s1)) - 8388736.0f;
+  return prmt(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+}
+
+// ---------------------------------------------------------------- tile loader
+template <int FMT>
+__device__ __forceinline__ void load_tile(const AttendParams& p, uint8_t* stage, const uint8_t* base, int slot0,
+                                          int g, int tid, int nthr) {
+  const CacheView& C = p.C;
+  const uint32_t s = smem_u32(stage);
+  const int H = C.H;
+  // K codes: 16 cells x 16 chunks; chunk kk of cell j stored at kk ^ (4 * (j & 1))
+  for (int i = tid; i < 256; i += nthr) {
+    const int j = i >> 4, kk = i & 15;
+    const uint8_t* src = base + (static_cast<int64_t>(slot0 + j) * H + g) * 256 + 16 * kk;
+    cp_async16(s + Stage<FMT>::kK + j * 256 + 16 * (kk ^ ((j & 1) << 2)), src);
+  }
+  if (FMT == K8V4_FORMAT_K8V4) {
+    // V nibbles: 16 cells x 8 blocks; block b of cell j stored at b ^ (j & 7)
+    for (int i = tid; i < 128; i += nthr) {
+      const int j = i >> 3, bb = i & 7;
+      const uint8_t* src = base + C.v_off() + (static_cast<int64_t>(slot0 + j) * H + g) * 128 + 16 * bb;
+      cp_async16(s + Stage<FMT>::kV + j * 128 + 16 * (bb ^ (j & 7)), src);
+    }
+  } else {
+    for (int i = tid; i < 256; i += nthr) {
+      const int j = i >> 4, kk = i & 15;
+      const uint8_t* src = base + C.v_off() + (static_cast<int64_t>(slot0 + j) * H + g) * 256 + 16 * kk;
+      cp_async16(s + Stage<FMT>::kV + j * 256 + 16 * (kk ^ (j & 7)), src);
+    }
+  }
+  for (int i = tid; i < 32; i += nthr) {
+    const int j = i & 15;
+    const int64_t r = static_cast<int64_t>(slot0 + j) * H + g;
+    if (i < 16) {
+      cp_async8(s + Stage<FMT>::kKs + 8 * j, base + C.ks_off() + r * 8);
+    } else if (FMT == K8V4_FORMAT_K8V4) {
+      cp_async16(s + Stage<FMT>::kVs + 16 * j, base + C.vs_off() + r * 16);
+    } else {
+      cp_async8(s + Stage<FMT>::kVs + 8 * j, base + C.vs_off() + r * 8);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- main kernel
+template <int FMT, bool QF32>
+__global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using S = Stage<FMT>;
+  constexpr int kMT = 16;                                 // PV m-tiles (16 dims each)
+  constexpr int kBlocks = FMT == K8V4_FORMAT_K8V4 ? 8 : 2; // scale blocks per head
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int qi = warp % p.n_q, gi = warp / p.n_q;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int r0 = lane >> 2, c = lane & 3;
+  const CacheView& C = p.C;
+  const int HQ = C.H * kGqa;
+
+  // ---- visible counts (device values, clipped to the host bound)
+  int n_max = 0, n_vis = 0;
+  for (int i = 0; i < p.n_q; ++i) {
+    int v = p.steps[static_cast<int64_t>(b) * p.n_q + i];
+    if (v < 0 || v > p.max_seq_len) {
+      if (threadIdx.x == 0 && split == 0 && g == 0) record_status(p.status, K8V4_ERANGE);
+      v = v < 0 ? 0 : p.max_seq_len;
+    }
+    n_max = max(n_max, v);
+    if (i == qi) n_vis = v;
+  }
+  const int c_begin = split * p.cells_per_split;
+  const int c_stop = c_begin + p.cells_per_split;
+  const int c_end = min(c_stop, n_max);
+  const int n_tiles = c_end > c_begin ? (c_end - c_begin + 15) >> 4 : 0;
+  const int lim = min(n_vis, c_stop);       // this query's cells in this split end here
+
+  // ---- q fragments (B operand of QK^T): lane holds head r0, dims 64i + 16c + 4j + e
+  uint32_t qf[16][2];
+  uint32_t qf_lo[QF32 ? 16 : 1][2];
+  float fscale;                                    // per head: sm_scale * log2(e) / 2^qexp
+  {
+    const int64_t qrow = ((static_cast<int64_t>(b) * p.n_q + qi) * HQ + g * kGqa + r0) * kD;
+    float qv[64];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t e0 = qrow + 64 * i + 16 * c;
+      if (QF32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + e0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float4 v4 = src[t];
+          qv[16 * i + 4 * t] = v4.x; qv[16 * i + 4 * t + 1] = v4.y;
+          qv[16 * i + 4 * t + 2] = v4.z; qv[16 * i + 4 * t + 3] = v4.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + e0);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint4 raw = src[t];
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            qv[16 * i + 8 * t + 2 * u] = __uint_as_float(w[u] << 16);
+            qv[16 * i + 8 * t + 2 * u + 1] = __uint_as_float(w[u] & 0xffff0000u);
+          }
+        }
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 64; ++t) amax = fmaxf(amax, fabsf(qv[t]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    int ex = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 : 0;
+    int sh = 14 - ex;                               // amax * 2^sh in [2^14, 2^15)
+    sh = max(-100, min(100, sh));
+    const float up = ldexpf(1.0f, sh);
+    fscale = p.sm_scale_log2 * ldexpf(1.0f, -sh);
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {
+      const int o = 16 * (ks >> 2) + 4 * (ks & 3);
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(qv[o + e], up);
+      const __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+      qf[ks][0] = *reinterpret_cast<const uint32_t*>(&h0);
+      qf[ks][1] = *reinterpret_cast<const uint32_t*>(&h1);
+      if (QF32) {
+        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+        const __half2 l0 = __floats2half2_rn(v[0] - f0.x, v[1] - f0.y);
+        const __half2 l1 = __floats2half2_rn(v[2] - f1.x, v[3] - f1.y);
+        qf_lo[ks % (QF32 ? 16 : 1)][0] = *reinterpret_cast<const uint32_t*>(&l0);
+        qf_lo[ks % (QF32 ? 16 : 1)][1] = *reinterpret_cast<const uint32_t*>(&l1);
+      }
+    }
+  }
+  // score factors for the heads of the C layout (2c, 2c+1): held by lanes 4h
+  const float f0 = __shfl_sync(kFull, fscale, 8 * c), f1 = __shfl_sync(kFull, fscale, 8 * c + 4);
+
+  float o[kMT][4];
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+  // ---- pipeline over this group's tiles: gi, gi + n_groups, ...
+  uint8_t* gbuf = smem + static_cast<size_t>(gi) * kStages * S::kBytes;
+  const int n_my = n_tiles > gi ? (n_tiles - gi + p.n_groups - 1) / p.n_groups : 0;
+  const int tid = qi * 32 + lane, nthr = p.n_q * 32;
+  auto tile_page = [&](int t, int& slot0) -> const uint8_t* {
+    const int cell0 = c_begin + 16 * (gi + t * p.n_groups);
+    const int64_t pidx = cell0 / C.P;
+    slot0 = cell0 % C.P;
+    if (pidx >= p.max_pages) return nullptr;
+    const int64_t page = p.pt[static_cast<int64_t>(b) * p.max_pages + pidx];
+    if (page < 0 || page >= C.n_pages) return nullptr;
+    return C.pages + page * C.page_bytes;
+  };
+#pragma unroll 1
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < n_my) {
+      int slot0;
+      const uint8_t* base = tile_page(s, slot0);
+      if (base) load_tile<FMT>(p, gbuf + s * S::kBytes, base, slot0, g, tid, nthr);
+      else if (tid == 0) record_status(p.status, K8V4_ERANGE);
+    }
+    cp_async_commit();
+  }
+#pragma unroll 1
+  for (int it = 0; it < n_my; ++it) {
+    cp_async_wait<kStages - 2>();
+    named_barrier(1 + gi, nthr);
+    {
+      const int nx = it + kStages - 1;
+      if (nx < n_my) {
+        int slot0;
+        const uint8_t* base = tile_page(nx, slot0);
+        if (base) load_tile<FMT>(p, gbuf + (nx % kStages) * S::kBytes, base, slot0, g, tid, nthr);
+        else if (tid == 0) record_status(p.status, K8V4_ERANGE);
+      }
+      cp_async_commit();
+    }
+    int slot_unused;
+    const bool valid = tile_page(it, slot_unused) != nullptr;
+    const int cell0 = c_begin + 16 * (gi + it * p.n_groups);
+    if (!valid || cell0 >= lim) continue;      // nothing visible for this query
+    const uint8_t* st = gbuf + (it % kStages) * S::kBytes;
+    const uint32_t st_s = smem_u32(st);
+
+    // ---- QK^T: S^T[cell][head], halves accumulated separately
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 ka = lds128(st_s + S::kK + r0 * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
+      const uint4 kb = lds128(st_s + S::kK + (r0 + 8) * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
+      const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a[4];
+        codes_to_f16(wa[j], a[0], a[2]);
+        codes_to_f16(wb[j], a[1], a[3]);
+        float* acc = i < 2 ? a0 : a1;
+        mma_f16(acc, a, qf[4 * i + j][0], qf[4 * i + j][1]);
+        if (QF32) mma_f16(acc, a, qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][0], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][1]);
+      }
+    }
+    const float2 kA = *reinterpret_cast<const float2*>(st + S::kKs + 8 * r0);
+    const float2 kB = *reinterpret_cast<const float2*>(st + S::kKs + 8 * (r0 + 8));
+    const bool vA = cell0 + r0 < lim, vB = cell0 + r0 + 8 < lim;
+    float sc[4];
+    sc[0] = vA ? (kA.x * a0[0] + kA.y * a1[0]) * f0 : -INFINITY;
+    sc[1] = vA ? (kA.x * a0[1] + kA.y * a1[1]) * f1 : -INFINITY;
+    sc[2] = vB ? (kB.x * a0[2] + kB.y * a1[2]) * f0 : -INFINITY;
+    sc[3] = vB ? (kB.x * a0[3] + kB.y * a1[3]) * f1 : -INFINITY;
+
+    // ---- online softmax (heads 2c, 2c+1)
+    float t0 = fmaxf(sc[0], sc[2]), t1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, off));
+      t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, off));
+    }
+    const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);   // finite: cell0 is visible
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    float pr[4];
+    pr[0] = exp2f(sc[0] - mn0);
+    pr[1] = exp2f(sc[1] - mn1);
+    pr[2] = exp2f(sc[2] - mn0);
+    pr[3] = exp2f(sc[3] - mn1);
+    l0 = l0 * al0 + (pr[0] + pr[2]);
+    l1 = l1 * al1 + (pr[1] + pr[3]);
+    m0 = mn0;
+    m1 = mn1;
+    if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+      }
+    }
+
+    // ---- transpose p to the B layout: lane gets head r0, cells 2c, 2c+1, 2c+8, 2c+9
+    float P[4];
+    {
+      const uint32_t u0 = __float_as_uint(pr[0]), u1 = __float_as_uint(pr[1]);
+      const uint32_t u2 = __float_as_uint(pr[2]), u3 = __float_as_uint(pr[3]);
+      const uint32_t th0 = movmatrix_t(prmt(u0, u1, 0x7632u)), tl0 = movmatrix_t(prmt(u0, u1, 0x5410u));
+      const uint32_t th1 = movmatrix_t(prmt(u2, u3, 0x7632u)), tl1 = movmatrix_t(prmt(u2, u3, 0x5410u));
+      P[0] = __uint_as_float(prmt(tl0, th0, 0x5410u));
+      P[1] = __uint_as_float(prmt(tl0, th0, 0x7632u));
+      P[2] = __uint_as_float(prmt(tl1, th1, 0x5410u));
+      P[3] = __uint_as_float(prmt(tl1, th1, 0x7632u));
+    }
+    const int pc[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+
+    // ---- PV in rotated space
+    if (FMT == K8V4_FORMAT_K8V4) {
+      uint4 dv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) dv[t] = *reinterpret_cast<const uint4*>(st + S::kVs + 16 * pc[t]);
+      const int mi = lane >> 3, rr = lane & 7;
+      const int lcell = rr + 8 * (mi & 1);
+#pragma unroll
+      for (int bp = 0; bp < 8; bp += 2) {
+        uint32_t R[4];
+        ldmatrix_x4_t(R, st_s + S::kV + lcell * 128 + 16 * ((bp + (mi >> 1)) ^ (lcell & 7)));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int bl = bp + h;
+          float x[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t word = (bl >> 1) == 0 ? dv[t].x : (bl >> 1) == 1 ? dv[t].y : (bl >> 1) == 2 ? dv[t].z : dv[t].w;
+            const __half dh = __ushort_as_half(static_cast<unsigned short>((bl & 1) ? (word >> 16) : (word & 0xffffu)));
+            x[t] = P[t] * __half2float(dh);
+          }
+          uint32_t B[kPlanes][2];
+#pragma unroll
+          for (int pl = 0; pl < kPlanes; ++pl) {
+            B[pl][0] = pack_bf16(x[0], x[1]);
+            B[pl][1] = pack_bf16(x[2], x[3]);
+            if (pl + 1 < kPlanes) {
+              x[0] -= bf16_lo(B[pl][0]); x[1] -= bf16_hi(B[pl][0]);
+              x[2] -= bf16_lo(B[pl][1]); x[3] -= bf16_hi(B[pl][1]);
+            }
+          }
+          const uint32_t Ra = R[2 * h], Rb = R[2 * h + 1];
+          uint32_t alo[4] = {nib_to_bf16(Ra, 0), nib_to_bf16(Ra, 8), nib_to_bf16(Rb, 0), nib_to_bf16(Rb, 8)};
+          uint32_t ahi[4] = {nib_to_bf16(Ra, 4), nib_to_bf16(Ra, 12), nib_to_bf16(Rb, 4), nib_to_bf16(Rb, 12)};
+#pragma unroll
+          for (int pl = 0; pl < kPlanes; ++pl) {
+            mma_bf16(o[2 * bl], alo, B[pl][0], B[pl][1]);
+            mma_bf16(o[2 * bl + 1], ahi, B[pl][0], B[pl][1]);
+          }
+        }
+      }
+    } else {
+      float sv[4][2];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 v2 = *reinterpret_cast<const float2*>(st + S::kVs + 8 * pc[t]);
+        sv[t][0] = v2.x;
+        sv[t][1] = v2.y;
+      }
+      const int mi = lane >> 3, rr = lane & 7;
+      const int lcell = rr + 8 * (mi & 1);
+#pragma unroll
+      for (int half = 0; half < kBlocks; ++half) {
+        float x[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) x[t] = P[t] * sv[t][half];
+        uint32_t B[kPlanes][2];
+#pragma unroll
+        for (int pl = 0; pl < kPlanes; ++pl) {
+          B[pl][0] = pack_bf16(x[0], x[1]);
+          B[pl][1] = pack_bf16(x[2], x[3]);
+          if (pl + 1 < kPlanes) {
+            x[0] -= bf16_lo(B[pl][0]); x[1] -= bf16_hi(B[pl][0]);
+            x[2] -= bf16_lo(B[pl][1]); x[3] -= bf16_hi(B[pl][1]);
+          }
+        }
+#pragma unroll
+        for (int mp = 0; mp < 8; mp += 2) {
+          const int mt0 = 8 * half + mp;
+          uint32_t R[4];
+          ldmatrix_x4_t(R, st_s + S::kV + lcell * 256 + 16 * ((mt0 + (mi >> 1)) ^ (lcell & 7)));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t Ra = R[2 * h], Rb = R[2 * h + 1];
+            uint32_t a[4] = {i8_to_bf16(Ra, 0x7540u, 0x7542u), i8_to_bf16(Ra, 0x7541u, 0x7543u),
+                             i8_to_bf16(Rb, 0x7540u, 0x7542u), i8_to_bf16(Rb, 0x7541u, 0x7543u)};
+#pragma unroll
+            for (int pl = 0; pl < kPlanes; ++pl) mma_bf16(o[mt0 + h], a, B[pl][0], B[pl][1]);
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // ---- finish: row sums across the 8 lanes of each head, then the CTA merge
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, off);
+    l1 += __shfl_xor_sync(kFull, l1, off);
+  }
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(smem);                 // [warps][8 * 256 + 16]
+  constexpr int kWS = 8 * 256 + 16;
+  float* mine = mo + static_cast<size_t>(warp) * kWS;
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt) {
+    int d0;
+    if (FMT == K8V4_FORMAT_K8V4) d0 = 32 * (mt >> 1) + 16 * (mt & 1) + 2 * r0;
+    else d0 = 16 * mt + 2 * r0;
+    *reinterpret_cast<float2*>(mine + (2 * c) * 256 + d0) = make_float2(o[mt][0], o[mt][2]);
+    *reinterpret_cast<float2*>(mine + (2 * c + 1) * 256 + d0) = make_float2(o[mt][1], o[mt][3]);
+  }
+  if (r0 == 0) {
+    mine[2048 + 2 * c] = m0;
+    mine[2048 + 2 * c + 1] = m1;
+    mine[2056 + 2 * c] = l0;
+    mine[2056 + 2 * c + 1] = l1;
+  }
+  __syncthreads();
+  const int total = p.n_q * 8 * 256;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int q2 = idx >> 11, h = (idx >> 8) & 7, dim = idx & 255;
+    float M = -INFINITY;
+    for (int gg = 0; gg < p.n_groups; ++gg) M = fmaxf(M, mo[static_cast<size_t>(gg * p.n_q + q2) * kWS + 2048 + h]);
+    float acc = 0.0f, L = 0.0f;
+    if (M != -INFINITY) {
+      for (int gg = 0; gg < p.n_groups; ++gg) {
+        const float* src = mo + static_cast<size_t>(gg * p.n_q + q2) * kWS;
+        const float mg = src[2048 + h];
+        if (mg == -INFINITY) continue;
+        const float sc2 = exp2f(mg - M);
+        acc += src[h * 256 + dim] * sc2;
+        L += src[2056 + h] * sc2;
+      }
+    }
+    float* dst = p.ws + ((((static_cast<int64_t>(b) * p.splits + split) * p.n_q + q2) * HQ) + g * kGqa + h) * kPStride;
+    dst[dim] = acc;
+    if (dim == 0) {
+      dst[256] = M;
+      dst[257] = L;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+template <int FMT>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws, int splits, int n_q, int HQ,
+                                                      float* __restrict__ out) {
+  __shared__ float red[8][260];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row = blockIdx.x;                 // (b, qi, head)
+  const int head = row % HQ;
+  const int bq = row / HQ;                    // b * n_q + qi
+  const int b = bq / n_q, qi = bq % n_q;
+  float M = -INFINITY, L = 0.0f, acc[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+  for (int s = warp; s < splits; s += 8) {
+    const float* src = ws + (((static_cast<int64_t>(b) * splits + s) * n_q + qi) * HQ + head) * kPStride;
+    const float ms = src[256];
+    if (ms == -INFINITY) continue;
+    const float ls = src[257];
+    const float4 x0 = reinterpret_cast<const float4*>(src + 8 * lane)[0];
+    const float4 x1 = reinterpret_cast<const float4*>(src + 8 * lane)[1];
+    const float Mn = fmaxf(M, ms);
+    const float a = exp2f(M - Mn), bsc = exp2f(ms - Mn);
+    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = acc[r] * a + xs[r] * bsc;
+    L = L * a + ls * bsc;
+    M = Mn;
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) red[warp][8 * lane + r] = acc[r];
+  if (lane == 0) {
+    red[warp][256] = M;
+    red[warp][257] = L;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) Mt = fmaxf(Mt, red[w][256]);
+  float v[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = 0.0f;
+  float Lt = 0.0f;
+  if (Mt != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float mw = red[w][256];
+      if (mw == -INFINITY) continue;
+      const float sc = exp2f(mw - Mt);
+      Lt += red[w][257] * sc;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) v[r] += red[w][8 * lane + r] * sc;
+    }
+  }
+  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] *= inv;
+  if (FMT == K8V4_FORMAT_K8V4) {
+    // out = (H/16) o: fast Walsh-Hadamard transform over element 8 * lane + r
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r & h) continue;
+        const float a = v[r], bb = v[r + h];
+        v[r] = a + bb;
+        v[r + h] = a - bb;
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float t = __shfl_xor_sync(kFull, v[r], m);
+        v[r] = upper ? t - v[r] : v[r] + t;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) v[r] *= 0.0625f;
+  }
+  float* dst = out + static_cast<int64_t>(row) * kD + 8 * lane;
+  reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+template <int FMT, bool QF32>
+int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, float* out) {
+  const size_t stage_bytes = static_cast<size_t>(plan.n_groups) * kStages * Stage<FMT>::kBytes;
+  const size_t merge_bytes = static_cast<size_t>(plan.warps) * (8 * 256 + 16) * sizeof(float);
+  const size_t smem = stage_bytes > merge_bytes ? stage_bytes : merge_bytes;
+  auto kern = attend_splitk_kernel<FMT, QF32>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return K8V4_ECUDA;
+  const dim3 grid(plan.splits, p.C.H, p.n_seqs);
+  kern<<<grid, plan.warps * 32, smem, L.stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
+  const int rows = p.n_seqs * p.n_q * p.C.H * kGqa;
+  combine_kernel<FMT><<<rows, 256, 0, L.stream>>>(p.ws, plan.splits, p.n_q, p.C.H * kGqa, out);
+  return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
+}
+
+}  // namespace
+
+AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
+  AttendPlan pl{};
+  pl.n_q = n_q;
+  pl.n_groups = n_q >= 8 ? 1 : 8 / n_q;
+  pl.warps = pl.n_groups * n_q;
+  const int tiles = max(1, (max_seq_len + 15) / 16);
+  const int stage_bytes = pl.n_groups * kStages * (C.fmt == K8V4_FORMAT_K8V4 ? Stage<K8V4_FORMAT_K8V4>::kBytes
+                                                                               : Stage<K8V4_FORMAT_INT8>::kBytes);
+  const int ctas_per_sm = max(1, min(4, (200 * 1024) / max(stage_bytes, 1)));
+  const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
+  const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm;
+  int64_t splits = (target + pairs - 1) / pairs;
+  const int64_t max_splits = std::max(1, tiles / (2 * pl.n_groups));
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, max_splits));
+  const int tps = static_cast<int>((tiles + splits - 1) / splits);
+  pl.cells_per_split = 16 * tps;
+  pl.splits = (tiles + tps - 1) / tps;
+  pl.ws_bytes = static_cast<size_t>(n_seqs) * pl.splits * n_q * C.H * kGqa * kPStride * sizeof(float);
+  return pl;
+}
+
+int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
+                  const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
+                  float sm_scale, float* out, void* ws) {
+  if (n_seqs == 0) return K8V4_OK;
+  AttendParams p;
+  p.C = C;
+  p.q = q;
+  p.pt = pt;
+  p.max_pages = max_pages;
+  p.steps = steps;
+  p.n_seqs = n_seqs;
+  p.n_q = plan.n_q;
+  p.n_groups = plan.n_groups;
+  p.max_seq_len = max_seq_len;
+  p.cells_per_split = plan.cells_per_split;
+  p.splits = plan.splits;
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.ws = static_cast<float*>(ws);
+  p.status = L.status;
+  const bool f32 = q_dtype == K8V4_F32;
+  if (C.fmt == K8V4_FORMAT_K8V4)
+    return f32 ? launch_impl<K8V4_FORMAT_K8V4, true>(L, p, plan, out) : launch_impl<K8V4_FORMAT_K8V4, false>(L, p, plan, out);
+  return f32 ? launch_impl<K8V4_FORMAT_INT8, true>(L, p, plan, out) : launch_impl<K8V4_FORMAT_INT8, false>(L, p, plan, out);
+}
+
+}  // namespace k8v4

@@ -1,0 +1,98 @@
+// Internal definitions shared by the k8v4 CUDA translation units: the device
+// view of a cache, the page-layout offsets, the device status word, small PTX
+// wrappers, and the host-side launch functions the C ABI calls.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/k8v4.h"
+
+namespace k8v4 {
+
+constexpr int kD = 256;   // head_dim
+constexpr int kGqa = 8;   // query heads per KV head
+
+// Bytes per (cell, head) of each format.  K8V4: 256 K codes + 8 (two fp32
+// scales) + 128 V nibbles + 16 (eight fp16 scales) = 408; INT8: 256 + 8 + 256 + 8.
+__host__ __device__ constexpr int cell_head_bytes(int fmt) { return fmt == K8V4_FORMAT_K8V4 ? 408 : 528; }
+
+// Device view of a cache.  Page p starts at pages + p * page_bytes; inside it
+// the runs are K codes [P][H][256], K scales [P][H][2] f32, V (nibbles
+// [P][H][8][16] or int8 codes [P][H][256]) and V scales ([P][H][8] f16 or
+// [P][H][2] f32).  r = slot * H + head indexes a (cell, head) inside a run.
+struct CacheView {
+  uint8_t* pages;
+  int64_t n_pages;
+  int64_t page_bytes;
+  int P;
+  int H;
+  int fmt;
+
+  __host__ __device__ int64_t ks_off() const { return 256ll * H * P; }
+  __host__ __device__ int64_t v_off() const { return 264ll * H * P; }
+  __host__ __device__ int64_t vs_off() const { return (fmt == K8V4_FORMAT_K8V4 ? 392ll : 520ll) * H * P; }
+  __host__ __device__ int v_row_bytes() const { return fmt == K8V4_FORMAT_K8V4 ? 128 : 256; }
+  __host__ __device__ int vs_row_bytes() const { return fmt == K8V4_FORMAT_K8V4 ? 16 : 8; }
+};
+
+// ---------------------------------------------------------------- status word
+// Kernels record the first device-side error here (compare-and-swap from 0) and
+// skip the offending access; the host reads and clears it.
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- host side
+struct Launch {
+  cudaStream_t stream;
+  int* status;      // device status word of the current device
+  int num_sms;
+};
+
+int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_t max_pages, int n_seqs,
+                  const int64_t* pos, int n_tok, const void* k, const void* v, int dtype);
+int launch_dequant(const Launch& L, const CacheView& C, const int32_t* pt, int64_t max_pages, int64_t start,
+                   int64_t n_cells, float* k_out, float* v_rot_out, float* v_out);
+
+struct AttendPlan {
+  int n_q, n_groups, warps, splits, cells_per_split;
+  size_t ws_bytes;
+};
+AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms);
+int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
+                  const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
+                  float sm_scale, float* out, void* ws);
+int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,
+                   int seq_len, int n_q_tok, const int32_t* steps, float sm_scale, float* out);
+
+}  // namespace k8v4

@@ -1,0 +1,394 @@
+"""Benchmark of the k8v4 decode hot path on GB300.
+
+Workload (the 238K point of the long-context sweep): one sequence of 237,568
+cells, 2 KV heads x 256, 16 query heads (GQA 8), page size 64, shuffled page
+table, bf16 K/V/q N(0,1) with 3 outlier channels per head x20.  One step is the
+engine's decode step: append the newest token's K/V (quantise + paged write)
+and run split-K decode attention over all 237,568 cells (partials + combine with
+the inverse Walsh-Hadamard transform).  Two cache replicas alternate between
+steps (388 MB > L2), so every step streams its cache from HBM.
+
+Metric: decode-attention GB/s over 816 B/cell (and cells/s); the same line also
+reports append cells/s (bulk append of the whole cache, 2,864 B/cell of
+algorithmic traffic), the INT8/INT8 comparison arm (1,056 B/cell), the roofline
+of the decode call, the end-to-end rate through the C ABI with host buffers, and
+the CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl k8v4|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path
+has no exchange step); value = cells of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_CELLS = 237568
+P = 64
+H = 2
+HQ = 16
+CELL_BYTES = 816
+CELL_BYTES_INT8 = 1056
+APPEND_BYTES = 2 * H * 256 * 2 + CELL_BYTES      # bf16 K+V in, 816 B out
+METRIC = "k8v4 decode-attn GB/s (% HBM peak) and cells/s @238K ctx; append cells/s"
+WORKLOAD = "decode_237568_cells_2kv_16q_gqa8_P64_bf16"
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_dram.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "quantized_paged_kv_q8_gb300", "csrc", fields.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != fields.get("source_sha256_16"):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.05)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_decode_rate(w, n_cells: int, repeats: int, n_threads: int):
+    """Time the CPU oracle's decode attention (16 rows) over the first n_cells of
+    the workload, its cache built by its own append (untimed).  Returns GB/s over
+    816 B/cell, seconds per step."""
+    import oracle
+    n_pages = (n_cells + P - 1) // P
+    pt = np.arange(n_pages, dtype=np.int32)[None]
+    cache = oracle.Cache(n_pages, P, H)
+    cache.append(pt, np.array([0]), w.k.f32[None, :n_cells], w.v.f32[None, :n_cells], n_threads=n_threads)
+    rs, rh, rv = oracle.decode_rows(1, HQ, [n_cells])
+    q = w.q.f32.reshape(-1, 256)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        cache.attention(pt, rs, rh, rv, q, n_threads=n_threads)
+    dt = (time.perf_counter() - t0) / repeats
+    return CELL_BYTES * n_cells / dt / 1e9, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import synth
+    threads = os.cpu_count() or 1
+    w = synth.config3(N_CELLS)
+    # size each step so that warmup + steps end within about two minutes
+    _, t_small = oracle_decode_rate(w, 4096, 1, threads)
+    per_cell = t_small / 4096
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_cells = int(min(N_CELLS, max(1024, budget / per_cell)) // P * P)
+    import oracle
+    n_pages = n_cells // P
+    pt = np.arange(n_pages, dtype=np.int32)[None]
+    cache = oracle.Cache(n_pages, P, H)
+    cache.append(pt, np.array([0]), w.k.f32[None, :n_cells], w.v.f32[None, :n_cells], n_threads=threads)
+    rs, rh, rv = oracle.decode_rows(1, HQ, [n_cells])
+    q = w.q.f32.reshape(-1, 256)
+    for _ in range(args.warmup):
+        cache.attention(pt, rs, rh, rv, q, n_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cache.attention(pt, rs, rh, rv, q, n_threads=threads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = CELL_BYTES * n_cells / dt / 1e9
+    sample = (f"per step: CPU oracle fp64 decode attention, 16 query rows over the first {n_cells} of the "
+              f"{N_CELLS}-cell workload (its cache built by its own append, untimed); GB/s over 816 B/cell")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "cells": N_CELLS, "sample_cells": n_cells},
+            "cells_per_s": n_cells / dt,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="k8v4", choices=["k8v4", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="lean run for ncu: one cache replica, no INT8 arm / e2e / CPU baseline")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import quantized_paged_kv_q8_gb300 as k8
+    import synth
+    from quantized_paged_kv_q8_gb300 import buildlib
+    buildlib.build()
+    assert k8.k8v4_device_check() == 0, "libk8v4 needs an sm_103 device"
+
+    w = synth.config3(N_CELLS)
+    n_pages = w.n_pages
+    pt = torch.from_numpy(w.page_table).to(dev)
+    kd = torch.from_numpy(w.k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, N_CELLS, H, 256).to(dev)
+    vd = torch.from_numpy(w.v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, N_CELLS, H, 256).to(dev)
+    zero = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- bulk append (cache build) timing: append cells/s
+    n_rep = 1 if args.profile else 2
+    caches = [k8.PagedCache(n_pages, P, H, device=dev) for _ in range(n_rep)]
+    for c in caches:
+        k8.kv_append_k8v4(c, pt, zero, kd, vd)
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_app = 5
+    a0.record()
+    for i in range(n_app):
+        k8.kv_append_k8v4(caches[i % n_rep], pt, zero, kd, vd)
+    a1.record()
+    torch.cuda.synchronize()
+    append_s = a0.elapsed_time(a1) / 1e3 / n_app
+    assert k8.k8v4_last_device_status() == 0
+
+    # ---- decode step inputs
+    q = torch.from_numpy(w.q.dev.view(np.int16)).view(torch.bfloat16).reshape(1, HQ, 256).to(dev)
+    pos_last = torch.full((1,), N_CELLS - 1, dtype=torch.int64, device=dev)
+    k_new = kd[:, N_CELLS - 1:].contiguous()
+    v_new = vd[:, N_CELLS - 1:].contiguous()
+    lens = torch.full((1,), N_CELLS, dtype=torch.int32, device=dev)
+    out = torch.empty(1, HQ, 256, dtype=torch.float32, device=dev)
+    wsp = k8.workspace(caches[0], 1, 1, N_CELLS, device=dev)
+
+    if args.profile:
+        del kd, vd
+        torch.cuda.empty_cache()
+
+    def step(i):
+        c = caches[i % n_rep]
+        k8.kv_append_k8v4(c, pt, pos_last, k_new, v_new)
+        k8.attn_k8v4_decode(c, q, pt, lens, N_CELLS, out, wsp)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0.record()
+        for i in range(K):
+            c = caches[i % n_rep]
+            k8.kv_append_k8v4(c, pt, pos_last, k_new, v_new)
+            ev[i][0].record()
+            k8.attn_k8v4_decode(c, q, pt, lens, N_CELLS, out, wsp)
+            ev[i][1].record()
+        t1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    assert k8.k8v4_last_device_status() == 0
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / K
+    cells_per_s = world * N_CELLS / (ms_step / 1e3)
+    value = cells_per_s * CELL_BYTES / 1e9
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": True, "ms_per_step": ms_step, "decode_ms": dec_ms,
+                              "gbs": CELL_BYTES * N_CELLS / (dec_ms / 1e3) / 1e9}), flush=True)
+        return
+
+    # ---- INT8/INT8 comparison arm (1,056 B/cell), same workload
+    c8 = [k8.PagedCache(n_pages, P, H, fmt=k8.FORMAT_INT8, device=dev) for _ in range(2)]
+    for c in c8:
+        k8.kv_append_k8v4(c, pt, zero, kd, vd)
+    ws8 = k8.workspace(c8[0], 1, 1, N_CELLS, device=dev)
+    for i in range(20):
+        k8.attn_k8v4_decode(c8[i & 1], q, pt, lens, N_CELLS, out, ws8)
+    K8 = max(20, K // 5)
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record()
+    for i in range(K8):
+        k8.attn_k8v4_decode(c8[i & 1], q, pt, lens, N_CELLS, out, ws8)
+    b1.record()
+    torch.cuda.synchronize()
+    int8_ms = b0.elapsed_time(b1) / K8
+    del c8, ws8
+
+    # ---- end to end through the C ABI with host buffers
+    q_h = q.cpu().pin_memory()
+    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    q_s, kn_s, vn_s = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    Ke = max(20, min(K, 2000))
+
+    def e2e_step(i):
+        q_s.copy_(q_h, non_blocking=True)
+        kn_s.copy_(kn_h, non_blocking=True)
+        vn_s.copy_(vn_h, non_blocking=True)
+        c = caches[i % n_rep]
+        k8.kv_append_k8v4(c, pt, pos_last, kn_s, vn_s)
+        k8.attn_k8v4_decode(c, q_s, pt, lens, N_CELLS, out, wsp)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(10):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(Ke):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    h2d = q.numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2
+    d2h = out.numel() * 4
+
+    hbm, bf16, _, peak_kind = peaks()
+    dec_bytes = CELL_BYTES * N_CELLS
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    traffic = traffic_record("attend_splitk_decode_237568")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "storage": "int8 K + q4_0 V, 816 B/cell", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "cells": N_CELLS, "page_size": P, "n_kv_heads": H, "n_q_heads": HQ,
+                   "step": "append 1 token + split-K decode attention (partials + combine/inverse WHT)",
+                   "l2": "inputs larger than L2: two 193.9 MB cache replicas alternate (387.7 MB > 135.5 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "cells_per_s": cells_per_s,
+        "hbm_frac_of_step": value / hbm,
+        "roofline": {"bound": "hbm", "kernel": "attn_k8v4_decode (split-K partial + combine)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": dec_bytes,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)", "ms_per_launch": dec_ms},
+        "append": {"cells_per_s": N_CELLS / append_s, "gbs": APPEND_BYTES * N_CELLS / append_s / 1e9,
+                   "frac": APPEND_BYTES * N_CELLS / append_s / 1e9 / hbm, "bytes_per_cell": APPEND_BYTES,
+                   "ms_per_launch": append_s * 1e3, "cells_per_launch": N_CELLS},
+        "int8_arm": {"gbs": CELL_BYTES_INT8 * N_CELLS / (int8_ms / 1e3) / 1e9, "ms_per_step": int8_ms,
+                     "cells_per_s": N_CELLS / (int8_ms / 1e3), "bytes_per_cell": CELL_BYTES_INT8,
+                     "k8v4_speedup": int8_ms / dec_ms},
+        "e2e": {"value": dec_bytes / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        gbs, dt = oracle_decode_rate(w, N_CELLS, 3, threads)
+        line["cpu_baseline"] = {
+            "value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"one decode step (16 query rows) over the full {N_CELLS}-cell cache, 3 repeats, fp64 oracle; "
+                      f"its cache built by its own append (untimed); {dt:.2f} s per step"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -136,6 +136,26 @@ int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, co
                      int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
                      float sm_scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode attention that allocates nothing and takes no workspace.  The pages
+ * have no counterpart to this call; it exists for callers that cannot allocate
+ * device memory: a host with no device allocator of its own (a plain C program
+ * embedding the library on a fixed device budget handed out up front, or a
+ * framework whose memory pool already owns all device memory), or a loop that
+ * must not call cudaMalloc/cudaFree because cudaFree synchronises the device.
+ * Arguments and results are those of attn_k8v4_decode without the workspace.
+ * The split-K partials go to a 4 MiB array in the library's own device memory
+ * (every GPU that loads the library holds it until the process exits); calls
+ * whose attn_k8v4_workspace_bytes(cache, n_seqs, 1, max_seq_len) exceeds 4 MiB
+ * are rejected with K8V4_ENOSPACE before any launch.  The first call on a device
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture.  All calls share the one array: calls
+ * that overlap on the GPU (other streams, other host threads) race and corrupt
+ * each other's results, so serialise them.  Nothing in the array has to start
+ * at zero: each call writes every partial it reads. */
+int attn_k8v4_decode_noalloc(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
+                             int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
+                             float sm_scale, float* out, void* stream);
+
 /* Verify attention: n_q queries per sequence, query i of sequence b seeing
  * step_arrays[b][i] cells (the batched form with per-query step arrays, as
  * verify uses it, the k8v4 PR "Tests"; for a speculative window of 4 drafts + 1

@@ -59,6 +59,7 @@ def lib():
             "kv_append_k8v4": ([C, P, I64, I32, P, I32, P, P, I32, P], ctypes.c_int),
             "attn_k8v4_workspace_bytes": ([C, I32, I32, I32], SZ),
             "attn_k8v4_decode": ([C, P, I32, P, I64, P, I32, I32, F, P, P, SZ, P], ctypes.c_int),
+            "attn_k8v4_decode_noalloc": ([C, P, I32, P, I64, P, I32, I32, F, P, P], ctypes.c_int),
             "attn_k8v4_verify": ([C, P, I32, P, I64, P, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
             "attn_k8v4_prefill": ([C, P, I32, P, I64, I32, I32, P, F, P, P], ctypes.c_int),
             "kv_dequant_k8v4": ([C, P, I64, I64, I64, P, P, P, P], ctypes.c_int),
@@ -73,7 +74,8 @@ def lib():
 
 
 EXPORTED = ("k8v4_bytes_per_cell", "k8v4_status_string", "k8v4_device_check", "kv_append_k8v4",
-            "attn_k8v4_workspace_bytes", "attn_k8v4_decode", "attn_k8v4_verify", "attn_k8v4_prefill",
+            "attn_k8v4_workspace_bytes", "attn_k8v4_decode", "attn_k8v4_decode_noalloc", "attn_k8v4_verify",
+            "attn_k8v4_prefill",
             "kv_dequant_k8v4", "k8v4_last_device_status")
 
 

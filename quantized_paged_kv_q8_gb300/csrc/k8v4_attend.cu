@@ -29,9 +29,19 @@ namespace k8v4 {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kStages = 3;
+#ifndef K8V4_STAGES
+#define K8V4_STAGES 3
+#endif
+#ifndef K8V4_DECODE_WARPS
+#define K8V4_DECODE_WARPS 8
+#endif
+constexpr int kStages = K8V4_STAGES;          // cp.async stages per tile group
+constexpr int kWarps = K8V4_DECODE_WARPS;     // warps per CTA (tile groups x queries)
 constexpr int kPStride = 260;   // floats per partial row: o[256], m, l, 2 pad
-constexpr int kPlanes = 3;      // bf16 terms of p * d
+#ifndef K8V4_PV_PLANES
+#define K8V4_PV_PLANES 3
+#endif
+constexpr int kPlanes = K8V4_PV_PLANES;   // bf16 terms of p * d (3 = 24 significant bits)
 
 template <int FMT>
 struct Stage {
@@ -159,7 +169,7 @@ __device__ __forceinline__ void load_tile(const AttendParams& p, uint8_t* stage,
 
 // ---------------------------------------------------------------- main kernel
 template <int FMT, bool QF32>
-__global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const AttendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   using S = Stage<FMT>;
   constexpr int kMT = 16;                                 // PV m-tiles (16 dims each)
@@ -282,7 +292,8 @@ __global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParam
 #pragma unroll 1
   for (int it = 0; it < n_my; ++it) {
     cp_async_wait<kStages - 2>();
-    named_barrier(1 + gi, nthr);
+    if (nthr == 32) __syncwarp();          // a one-warp group needs no CTA barrier
+    else named_barrier(1 + gi, nthr);
     {
       const int nx = it + kStages - 1;
       if (nx < n_my) {
@@ -300,22 +311,34 @@ __global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParam
     const uint8_t* st = gbuf + (it % kStages) * S::kBytes;
     const uint32_t st_s = smem_u32(st);
 
-    // ---- QK^T: S^T[cell][head], halves accumulated separately
-    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- QK^T: S^T[cell][head], halves accumulated separately; two
+    // accumulators per half keep four independent MMA chains in flight
+    float acc[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint4 ka = lds128(st_s + S::kK + r0 * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
       const uint4 kb = lds128(st_s + S::kK + (r0 + 8) * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
       const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+      uint32_t a[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t a[4];
-        codes_to_f16(wa[j], a[0], a[2]);
-        codes_to_f16(wb[j], a[1], a[3]);
-        float* acc = i < 2 ? a0 : a1;
-        mma_f16(acc, a, qf[4 * i + j][0], qf[4 * i + j][1]);
-        if (QF32) mma_f16(acc, a, qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][0], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][1]);
+        codes_to_f16(wa[j], a[j][0], a[j][2]);
+        codes_to_f16(wb[j], a[j][1], a[j][3]);
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float* dst = acc[2 * (i >> 1) + (j & 1)];
+        mma_f16(dst, a[j], qf[4 * i + j][0], qf[4 * i + j][1]);
+        if (QF32) mma_f16(dst, a[j], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][0], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][1]);
+      }
+    }
+    float a0[4], a1[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      a0[t] = acc[0][t] + acc[1][t];
+      a1[t] = acc[2][t] + acc[3][t];
     }
     const float2 kA = *reinterpret_cast<const float2*>(st + S::kKs + 8 * r0);
     const float2 kB = *reinterpret_cast<const float2*>(st + S::kKs + 8 * (r0 + 8));
@@ -376,6 +399,8 @@ __global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParam
       for (int bp = 0; bp < 8; bp += 2) {
         uint32_t R[4];
         ldmatrix_x4_t(R, st_s + S::kV + lcell * 128 + 16 * ((bp + (mi >> 1)) ^ (lcell & 7)));
+        uint32_t B[2][kPlanes][2];
+        uint32_t alo[2][4], ahi[2][4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int bl = bp + h;
@@ -386,23 +411,27 @@ __global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParam
             const __half dh = __ushort_as_half(static_cast<unsigned short>((bl & 1) ? (word >> 16) : (word & 0xffffu)));
             x[t] = P[t] * __half2float(dh);
           }
-          uint32_t B[kPlanes][2];
 #pragma unroll
           for (int pl = 0; pl < kPlanes; ++pl) {
-            B[pl][0] = pack_bf16(x[0], x[1]);
-            B[pl][1] = pack_bf16(x[2], x[3]);
+            B[h][pl][0] = pack_bf16(x[0], x[1]);
+            B[h][pl][1] = pack_bf16(x[2], x[3]);
             if (pl + 1 < kPlanes) {
-              x[0] -= bf16_lo(B[pl][0]); x[1] -= bf16_hi(B[pl][0]);
-              x[2] -= bf16_lo(B[pl][1]); x[3] -= bf16_hi(B[pl][1]);
+              x[0] -= bf16_lo(B[h][pl][0]); x[1] -= bf16_hi(B[h][pl][0]);
+              x[2] -= bf16_lo(B[h][pl][1]); x[3] -= bf16_hi(B[h][pl][1]);
             }
           }
           const uint32_t Ra = R[2 * h], Rb = R[2 * h + 1];
-          uint32_t alo[4] = {nib_to_bf16(Ra, 0), nib_to_bf16(Ra, 8), nib_to_bf16(Rb, 0), nib_to_bf16(Rb, 8)};
-          uint32_t ahi[4] = {nib_to_bf16(Ra, 4), nib_to_bf16(Ra, 12), nib_to_bf16(Rb, 4), nib_to_bf16(Rb, 12)};
+          alo[h][0] = nib_to_bf16(Ra, 0); alo[h][1] = nib_to_bf16(Ra, 8);
+          alo[h][2] = nib_to_bf16(Rb, 0); alo[h][3] = nib_to_bf16(Rb, 8);
+          ahi[h][0] = nib_to_bf16(Ra, 4); ahi[h][1] = nib_to_bf16(Ra, 12);
+          ahi[h][2] = nib_to_bf16(Rb, 4); ahi[h][3] = nib_to_bf16(Rb, 12);
+        }
 #pragma unroll
-          for (int pl = 0; pl < kPlanes; ++pl) {
-            mma_bf16(o[2 * bl], alo, B[pl][0], B[pl][1]);
-            mma_bf16(o[2 * bl + 1], ahi, B[pl][0], B[pl][1]);
+        for (int pl = 0; pl < kPlanes; ++pl) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            mma_bf16(o[2 * (bp + h)], alo[h], B[h][pl][0], B[h][pl][1]);
+            mma_bf16(o[2 * (bp + h) + 1], ahi[h], B[h][pl][0], B[h][pl][1]);
           }
         }
       }
@@ -501,62 +530,63 @@ __global__ void __launch_bounds__(256, 1) attend_splitk_kernel(const AttendParam
 }
 
 // ---------------------------------------------------------------- combine
+// One CTA per output row (b, query, head); thread t owns rotated dim t.  The
+// split maxima are reduced first, then every thread sums its dim over the
+// splits with independent loads; one warp applies the inverse transform.
 template <int FMT>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws, int splits, int n_q, int HQ,
                                                       float* __restrict__ out) {
-  __shared__ float red[8][260];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ float red[256];
+  __shared__ float mx[8];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int row = blockIdx.x;                 // (b, qi, head)
   const int head = row % HQ;
   const int bq = row / HQ;                    // b * n_q + qi
   const int b = bq / n_q, qi = bq % n_q;
-  float M = -INFINITY, L = 0.0f, acc[8];
+  const int64_t stride = static_cast<int64_t>(n_q) * HQ * kPStride;    // between splits
+  const float* base = ws + ((static_cast<int64_t>(b) * splits * n_q + qi) * HQ + head) * kPStride;
+  float M = -INFINITY;
+  for (int s = t; s < splits; s += 256) M = fmaxf(M, base[s * stride + 256]);
 #pragma unroll
-  for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-  for (int s = warp; s < splits; s += 8) {
-    const float* src = ws + (((static_cast<int64_t>(b) * splits + s) * n_q + qi) * HQ + head) * kPStride;
-    const float ms = src[256];
-    if (ms == -INFINITY) continue;
-    const float ls = src[257];
-    const float4 x0 = reinterpret_cast<const float4*>(src + 8 * lane)[0];
-    const float4 x1 = reinterpret_cast<const float4*>(src + 8 * lane)[1];
-    const float Mn = fmaxf(M, ms);
-    const float a = exp2f(M - Mn), bsc = exp2f(ms - Mn);
-    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-    for (int r = 0; r < 8; ++r) acc[r] = acc[r] * a + xs[r] * bsc;
-    L = L * a + ls * bsc;
-    M = Mn;
-  }
-#pragma unroll
-  for (int r = 0; r < 8; ++r) red[warp][8 * lane + r] = acc[r];
-  if (lane == 0) {
-    red[warp][256] = M;
-    red[warp][257] = L;
-  }
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  if (lane == 0) mx[warp] = M;
   __syncthreads();
-  if (warp != 0) return;
-  float Mt = -INFINITY;
+  M = mx[0];
 #pragma unroll
-  for (int w = 0; w < 8; ++w) Mt = fmaxf(Mt, red[w][256]);
-  float v[8];
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, mx[w]);
+  float acc = 0.0f, L = 0.0f;
+  if (M != -INFINITY) {
+    int s = 0;
+    for (; s + 4 <= splits; s += 4) {
+      float ms[4], ls[4], xs[4];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) v[r] = 0.0f;
-  float Lt = 0.0f;
-  if (Mt != -INFINITY) {
+      for (int u = 0; u < 4; ++u) {
+        const float* src = base + (s + u) * stride;
+        ms[u] = src[256];
+        ls[u] = src[257];
+        xs[u] = src[t];
+      }
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const float mw = red[w][256];
-      if (mw == -INFINITY) continue;
-      const float sc = exp2f(mw - Mt);
-      Lt += red[w][257] * sc;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) v[r] += red[w][8 * lane + r] * sc;
+      for (int u = 0; u < 4; ++u) {
+        const float wgt = ms[u] == -INFINITY ? 0.0f : exp2f(ms[u] - M);
+        acc += xs[u] * wgt;
+        L += ls[u] * wgt;
+      }
+    }
+    for (; s < splits; ++s) {
+      const float* src = base + s * stride;
+      const float ms = src[256];
+      const float wgt = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+      acc += src[t] * wgt;
+      L += src[257] * wgt;
     }
   }
-  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+  red[t] = L > 0.0f ? acc / L : 0.0f;
+  __syncthreads();
+  if (warp != 0) return;
+  float v[8];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) v[r] *= inv;
+  for (int r = 0; r < 8; ++r) v[r] = red[8 * lane + r];
   if (FMT == K8V4_FORMAT_K8V4) {
     // out = (H/16) o: fast Walsh-Hadamard transform over element 8 * lane + r
 #pragma unroll
@@ -574,8 +604,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       const bool upper = (lane & m) != 0;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const float t = __shfl_xor_sync(kFull, v[r], m);
-        v[r] = upper ? t - v[r] : v[r] + t;
+        const float tt = __shfl_xor_sync(kFull, v[r], m);
+        v[r] = upper ? tt - v[r] : v[r] + tt;
       }
     }
 #pragma unroll
@@ -607,7 +637,8 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
 AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
   AttendPlan pl{};
   pl.n_q = n_q;
-  pl.n_groups = n_q >= 8 ? 1 : 8 / n_q;
+  pl.n_groups = n_q >= kWarps ? 1 : kWarps / n_q;
+  if (n_q > 1 && pl.n_groups > 15) pl.n_groups = 15;   // named barriers 1..15
   pl.warps = pl.n_groups * n_q;
   const int tiles = max(1, (max_seq_len + 15) / 16);
   const int stage_bytes = pl.n_groups * kStages * (C.fmt == K8V4_FORMAT_K8V4 ? Stage<K8V4_FORMAT_K8V4>::kBytes

@@ -1,10 +1,625 @@
-// Chunked-prefill attention (tcgen05 tensor cores).  Placeholder until the
-// tensor-core kernel lands: the call reports an invalid argument.
+// Chunked-prefill attention over the k8v4 paged cache on the 5th-generation
+// tensor cores (tcgen05 + TMEM): the prompt form of the hybrid-KV pull request's
+// fused attention ("How": mode 3 runs for decode, prefill and verify; q is not
+// rotated, the output is computed in rotated space and rotated back).
+//
+// One CTA owns 128 query rows = 16 tokens x the 8 query heads of one KV head
+// (GQA packing: all 128 rows read the same K/V), and sweeps the cells visible to
+// them in tiles of 64:
+//   1. 16-byte cp.async copies bring the tile's raw runs (int8 K, K scales, V
+//      nibbles, fp16 V scales) into shared memory (double-buffered);
+//   2. all 256 threads dequantise it into fp16 operand tiles in the 128-byte
+//      swizzled layouts tcgen05 reads: K codes (exact in fp16) K-major, and
+//      Vhat_rot = (q - 8) * d as two fp16 planes V1 = RN(Vhat), V2 = Vhat - V1
+//      (both exact), MN-major;
+//   3. one thread issues S_h = Q_h K_h^T for the two 128-lane halves (separate
+//      TMEM accumulators, because each half has its own K scale), M=128, N=64,
+//      K=16 per instruction, and commits to an mbarrier;
+//   4. all 16 warps (TMEM lane = row; four threads per row, 16 cells each) read
+//      S, apply the K scales and the online softmax (log2 domain), and write
+//      P * 2^7 back into TMEM (over S) as two fp16 planes P1 = RN(P),
+//      P2 = RN(P - P1) (22 significant bits);
+//   5. one thread issues O_tile = P1 V1 + P1 V2 + P2 V1 into a fresh TMEM
+//      accumulator (A from TMEM, M=128, N=256, K=16; the dropped P2 V2 term is
+//      below 2^-22 of the product), and every thread folds its 64 dims of
+//      O_tile into an fp32 register accumulator: o = o * alpha + O_tile.
+//      Accumulating all tiles inside TMEM instead would let the tensor core's
+//      per-instruction accumulation rounding build up over thousands of steps.
+// fp16 operands with one rounding would leave errors near 1e-4 at 2^18 cells,
+// above the 2e-5 bar; the split planes bring them to the fp32 level.
+// The epilogue divides by l, applies the inverse Walsh-Hadamard transform
+// (out = (H/16) o) per row and writes fp32 rows.
+//
+// Every mbarrier wait is bounded: on timeout the kernel records an error in the
+// device status word, stops issuing work, waits (bounded) for its own
+// outstanding copies and MMAs, frees its TMEM and returns.
 #include "k8v4_common.cuh"
 
 namespace k8v4 {
-int launch_prefill(const Launch&, const CacheView&, const void*, const int32_t*, int64_t, int, int,
-                   const int32_t*, float, float*) {
-  return K8V4_EINVAL;
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRows = 128;            // query rows per CTA (16 tokens x 8 heads)
+constexpr int kTokens = kRows / kGqa; // 16
+constexpr int kTileN = 64;            // cells per tile
+constexpr int kThreads = 512;
+
+// shared memory map (bytes); every operand tile 1024-byte aligned
+constexpr int kQOff = 0;                       // Q fp16 [4 chunks][128 rows][128 B]  = 65536
+constexpr int kKfOff = kQOff + 65536;          // K fp16 [4 chunks][64 cells][128 B]  = 32768
+constexpr int kVfOff = kKfOff + 32768;         // Vhat fp16 2 planes x [4 atoms][64 cells][128 B] = 65536
+constexpr int kRawK = 64 * 256;                // raw tile: K codes [64][256]
+constexpr int kRawV = 64 * 128;                //           V nibbles [64][128]
+constexpr int kRawKs = 64 * 8;                 //           K scales [64][2] f32
+constexpr int kRawVs = 64 * 16;                //           V scales [64][8] f16
+constexpr int kRawBytes = kRawK + kRawV + kRawKs + kRawVs;   // 26112
+constexpr int kRawOff = kVfOff + 65536;        // 2 raw stages
+constexpr int kBarOff = kRawOff + 2 * kRawBytes;             // mbarriers + tmem slot
+constexpr int kKsBufOff = kBarOff + 64;                      // K scales of the current tile [64][2] f32
+constexpr int kRedOff = kKsBufOff + 512;                     // [4][128] f32 exchange + [128] f32 factors
+constexpr int kSmemBytes = kRedOff + 2048 + 512;
+static_assert(kRawOff % 1024 == 0, "alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+// the epilogue reuses [kKfOff, kKfOff + 128 KB) as a fp32 [128][256] row buffer
+static_assert(kBarOff - kKfOff >= 128 * 256 * 4, "epilogue buffer");
+
+constexpr uint32_t kTmemCols = 512;    // S0 [0,64), S1 [64,128), O_tile [128,384); P1/P2 reuse [0,64)
+constexpr uint32_t kS0Col = 0, kS1Col = 64, kOCol = 128, kP1Col = 0, kP2Col = 32;
+constexpr float kPScale = 128.0f;      // P is stored as p * 2^7 (p <= 1 -> <= 2^7; keeps tiny p normal in fp16)
+constexpr uint32_t kSpinLimit = 1u << 22;     // ~1 s of try_wait polling
+
+struct PrefillParams {
+  CacheView C;
+  const uint16_t* q;       // bf16 [n_q_tok][HQ][256]
+  const int32_t* pt;       // [max_pages]
+  int64_t max_pages;
+  const int32_t* steps;    // [n_q_tok] or null
+  int seq_len, n_q_tok;
+  float sm_scale_log2;
+  float* out;
+  int* status;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+// Wait for the phase with parity `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor (128-byte swizzle).  lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3fffu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;            // descriptor version (sm_100 family)
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// A operand from tensor memory (lanes = rows, columns = packed fp16 pairs along K)
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float v[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float v[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+// byte offset of 16-byte unit u of row r in a 128-byte-swizzled tile of 128-byte rows
+__device__ __forceinline__ uint32_t swz(int row, int unit) {
+  return static_cast<uint32_t>(row * 128 + ((unit ^ (row & 7)) << 4));
+}
+// four int8 codes -> two fp16x2 (exact)
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a = prmt(u, 0x64646464u, 0x4140u), b = prmt(u, 0x64646464u, 0x4342u);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+// two nibbles at bits k and k+16 of t -> fp16x2 planes of (n - 8) * d:
+// v1 = RN((n - 8) d) and v2 = (n - 8) d - v1, exact (the fma's exact result is
+// representable: (n - 8) d has at most 14 significant bits, all on d's grid)
+__device__ __forceinline__ void nib_vhat(uint32_t t, int k, __half2 d2, uint32_t& v1, uint32_t& v2) {
+  uint32_t x = ((t >> k) & 0x000f000fu) | 0x64006400u;                       // 1024 + n
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+  const __half2 c = __hsub2(*reinterpret_cast<__half2*>(&x), bias);          // n - 8, exact
+  const __half2 a = __hmul2(c, d2);
+  const __half2 b = __hfma2(c, d2, __hneg2(a));
+  v1 = *reinterpret_cast<const uint32_t*>(&a);
+  v2 = *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// ---------------------------------------------------------------- the kernel
+// 16 warps.  Row r of the 128 query rows lives in TMEM lane r and is served by
+// four threads, one per "part" (tid = part * 128 + r): each part reads 16 of the
+// tile's 64 scores and owns 64 of the 256 output dims (its share of O stays in
+// registers as fp32 across tiles).
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = tid & (kRows - 1), part = tid >> 7;
+  const int g = blockIdx.y;
+  const int tok0 = blockIdx.x * kTokens;
+  const CacheView& C = p.C;
+  const int HQ = C.H * kGqa;
+
+  const uint32_t bar_s = sbase + kBarOff, bar_o = sbase + kBarOff + 8;
+  const uint32_t tmem_slot = sbase + kBarOff + 16;
+  int* nmax_s = reinterpret_cast<int*>(smem + kBarOff + 28);
+  float* red = reinterpret_cast<float*>(smem + kRedOff);           // [4][128] partial maxima / sums
+  float* fsc = reinterpret_cast<float*>(smem + kRedOff + 2048);    // [128] score factor per row
+
+  // ---- visibility of this thread's row
+  int my_vis = 0;
+  {
+    const int t = tok0 + row / kGqa;
+    if (t < p.n_q_tok) {
+      int v = p.steps ? p.steps[t] : p.seq_len - p.n_q_tok + t + 1;
+      if (v < 0 || v > p.seq_len) {
+        if (part == 0) record_status(p.status, K8V4_ERANGE);
+        v = v < 0 ? 0 : p.seq_len;
+      }
+      my_vis = v;
+    }
+  }
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    *nmax_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (part == 0 && my_vis > 0) atomicMax(nmax_s, my_vis);
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+
+  // ---- Q rows -> fp16 with a per-row power-of-two scale, swizzled K-major;
+  // the four parts of a row convert dims [64 part, 64 part + 64)
+  {
+    const int t = tok0 + row / kGqa, h = row % kGqa;
+    uint4 raw[8];
+    if (t < p.n_q_tok) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(t) * HQ + g * kGqa + h) * kD + 64 * part);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) raw[i] = src[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) raw[i] = make_uint4(0, 0, 0, 0);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[u] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[u] & 0xffff0000u)));
+      }
+    }
+    red[part * kRows + row] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(red[row], red[kRows + row]), fmaxf(red[2 * kRows + row], red[3 * kRows + row]));
+    const int ex = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 : 0;
+    const int sh = max(-100, min(100, 14 - ex));
+    const float up = ldexpf(1.0f, sh);
+    if (part == 0) fsc[row] = p.sm_scale_log2 * ldexpf(1.0f, -sh);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+      uint32_t hv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = __fmul_rn(__uint_as_float(w[u] << 16), up);
+        const float b = __fmul_rn(__uint_as_float(w[u] & 0xffff0000u), up);
+        const __half2 h2 = __floats2half2_rn(a, b);
+        hv[u] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      // dims 64 part + 8i .. +7: chunk = part, unit = i
+      sts128(sbase + kQOff + part * 16384 + swz(row, i), hv[0], hv[1], hv[2], hv[3]);
+    }
+  }
+  __syncthreads();
+  const float my_f = fsc[row];
+  const int n_max = *nmax_s;
+  const int n_tiles = (n_max + kTileN - 1) / kTileN;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kBarOff + 16);
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+
+  // ---- raw tile loader (all threads, 16-byte cp.async)
+  auto load_raw = [&](int tile, int stage) {
+    const int cell0 = tile * kTileN;
+    const int64_t pidx = cell0 / C.P;
+    const uint32_t dst = sbase + kRawOff + stage * kRawBytes;
+    if (pidx >= p.max_pages) return false;
+    const int64_t page = p.pt[pidx];
+    if (page < 0 || page >= C.n_pages) return false;
+    const int slot0 = cell0 % C.P;       // P is a multiple of 64 here
+    const uint8_t* base = C.pages + page * C.page_bytes;
+    for (int i = tid; i < 64 * 16; i += kThreads) {              // K codes
+      const int j = i >> 4, kk = i & 15;
+      cp_async16(dst + j * 256 + 16 * kk, base + (static_cast<int64_t>(slot0 + j) * C.H + g) * 256 + 16 * kk);
+    }
+    {                                                            // V nibbles: 64 cells x 8 blocks
+      const int j = tid >> 3, kk = tid & 7;
+      cp_async16(dst + kRawK + j * 128 + 16 * kk,
+                 base + C.v_off() + (static_cast<int64_t>(slot0 + j) * C.H + g) * 128 + 16 * kk);
+    }
+    if (tid < 64) {
+      const int64_t r = static_cast<int64_t>(slot0 + tid) * C.H + g;
+      cp_async8(dst + kRawK + kRawV + 8 * tid, base + C.ks_off() + r * 8);
+      cp_async16(dst + kRawK + kRawV + kRawKs + 16 * tid, base + C.vs_off() + r * 16);
+    }
+    return true;
+  };
+
+  bool ok_tile[2] = {false, false};
+  if (n_tiles > 0) ok_tile[0] = load_raw(0, 0);
+  cp_async_commit();
+  if (n_tiles > 1) ok_tile[1] = load_raw(1, 1);
+  cp_async_commit();
+
+  float o_run[64];                 // this part's 64 dims of the row's O (rotated space)
+#pragma unroll
+  for (int i = 0; i < 64; ++i) o_run[i] = 0.0f;
+  float m_run = -INFINITY, l_part = 0.0f;
+  uint32_t phase = 0;
+  bool failed = false;
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int stage = it & 1;
+    cp_async_wait<1>();
+    __syncthreads();
+    const bool valid = __syncthreads_and(ok_tile[stage] ? 1 : 0) != 0;
+    if (!valid && tid == 0) record_status(p.status, K8V4_ERANGE);
+    const uint32_t raw = sbase + kRawOff + stage * kRawBytes;
+    // ---- dequantise into the operand tiles
+    if (valid) {
+      for (int i = tid; i < 64 * 16; i += kThreads) {            // K: (cell j, 16-byte chunk kk)
+        const int j = i >> 4, kk = i & 15;
+        const uint4 w = lds128(raw + j * 256 + 16 * kk);
+        uint32_t h[8];
+        i8x4_to_f16(w.x, h[0], h[1]);
+        i8x4_to_f16(w.y, h[2], h[3]);
+        i8x4_to_f16(w.z, h[4], h[5]);
+        i8x4_to_f16(w.w, h[6], h[7]);
+        const int dim = 16 * kk, chunk = dim >> 6, unit = (dim & 63) >> 3;
+        const uint32_t dst = sbase + kKfOff + chunk * 8192;
+        sts128(dst + swz(j, unit), h[0], h[1], h[2], h[3]);
+        sts128(dst + swz(j, unit + 1), h[4], h[5], h[6], h[7]);
+      }
+      {                                                          // V: (cell j, block b)
+        const int j = tid >> 3, b = tid & 7;
+        const uint4 w = lds128(raw + kRawK + j * 128 + 16 * b);
+        const __half dh = *reinterpret_cast<const __half*>(smem + kRawOff + stage * kRawBytes + kRawK + kRawV +
+                                                              kRawKs + 16 * j + 2 * b);
+        const __half2 d2 = __halves2half2(dh, dh);
+        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+        uint32_t lo[2][8], hi[2][8];   // [plane] dims 32b + (0..15) and 32b + 16 + (0..15), 8 pairs each
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t t01 = prmt(ws4[q], 0u, 0x5140u);   // {b0, 0, b1, 0}
+          const uint32_t t23 = prmt(ws4[q], 0u, 0x5342u);   // {b2, 0, b3, 0}
+          nib_vhat(t01, 0, d2, lo[0][2 * q], lo[1][2 * q]);
+          nib_vhat(t23, 0, d2, lo[0][2 * q + 1], lo[1][2 * q + 1]);
+          nib_vhat(t01, 4, d2, hi[0][2 * q], hi[1][2 * q]);
+          nib_vhat(t23, 4, d2, hi[0][2 * q + 1], hi[1][2 * q + 1]);
+        }
+        const int atom = b >> 1, unit0 = 4 * (b & 1);
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl) {
+          const uint32_t dst = sbase + kVfOff + pl * 32768 + atom * 8192;
+          sts128(dst + swz(j, unit0), lo[pl][0], lo[pl][1], lo[pl][2], lo[pl][3]);
+          sts128(dst + swz(j, unit0 + 1), lo[pl][4], lo[pl][5], lo[pl][6], lo[pl][7]);
+          sts128(dst + swz(j, unit0 + 2), hi[pl][0], hi[pl][1], hi[pl][2], hi[pl][3]);
+          sts128(dst + swz(j, unit0 + 3), hi[pl][4], hi[pl][5], hi[pl][6], hi[pl][7]);
+        }
+      }
+      if (tid < 64)      // K scales of the tile (the raw stage is refilled below)
+        reinterpret_cast<float2*>(smem + kKsBufOff)[tid] =
+            reinterpret_cast<const float2*>(smem + kRawOff + stage * kRawBytes + kRawK + kRawV)[tid];
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (it + 2 < n_tiles) ok_tile[stage] = load_raw(it + 2, stage);
+    cp_async_commit();
+    if (!valid) continue;
+
+    // ---- S_h = Q_h K_h^T (fresh accumulators)
+    if (tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t idS = idesc_f16(128, 64, false, false);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int chunk = 2 * h + (kk >> 2);
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = smem_desc(sbase + kQOff + chunk * 16384 + off, 16, 1024);
+          const uint64_t b = smem_desc(sbase + kKfOff + chunk * 8192 + off, 16, 1024);
+          mma_f16(tmem + (h ? kS1Col : kS0Col), a, b, idS, kk > 0 ? 1u : 0u);
+        }
+      }
+      mma_commit(bar_s);
+    }
+    if (!mbar_wait(bar_s, phase & 1)) failed = true;
+    tc_fence_after();
+    if (__syncthreads_or(failed ? 1 : 0)) { failed = true; break; }
+
+    // ---- scores of this part's 16 cells, row maximum across the four parts
+    const int cell0 = it * kTileN;
+    float sc[16];
+    {
+      const float* ks = reinterpret_cast<const float*>(smem + kKsBufOff);
+      float a[16], b[16];
+      tmem_ld16(tmem + lane_base + kS0Col + 16 * part, a);
+      tmem_ld16(tmem + lane_base + kS1Col + 16 * part, b);
+      const int vis = my_vis - cell0 - 16 * part;   // cells [0, vis) of this part are visible
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int cc = 16 * part + c;
+        const float v = (ks[2 * cc] * a[c] + ks[2 * cc + 1] * b[c]) * my_f;
+        sc[c] = c < vis ? v : -INFINITY;
+        mx = fmaxf(mx, sc[c]);
+      }
+      red[part * kRows + row] = mx;
+    }
+    __syncthreads();
+    const float mt = fmaxf(fmaxf(red[row], red[kRows + row]), fmaxf(red[2 * kRows + row], red[3 * kRows + row]));
+    const float m_new = fmaxf(m_run, mt);
+    const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);   // 0 on the first visible tile
+    const float mu = m_new == -INFINITY ? 0.0f : m_new;
+    m_run = m_new;
+    {
+      float p1v[8], p2v[8];
+      float psum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        const float a = __fmul_rn(exp2f(sc[c] - mu), kPScale), b = __fmul_rn(exp2f(sc[c + 1] - mu), kPScale);
+        const __half2 h1 = __floats2half2_rn(a, b);
+        const float2 f1 = __half22float2(h1);
+        const __half2 h2 = __floats2half2_rn(a - f1.x, b - f1.y);
+        const float2 f2 = __half22float2(h2);
+        psum += (f1.x + f2.x) + (f1.y + f2.y);  // l sums the probabilities the MMAs use
+        p1v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
+        p2v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+      }
+      l_part = l_part * alpha + psum;
+      // P planes overwrite S0's columns: every part has read its scores (barrier above)
+      tmem_st8(tmem + lane_base + kP1Col + 8 * part, p1v);
+      tmem_st8(tmem + lane_base + kP2Col + 8 * part, p2v);
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- O_tile = P1 V1 + P1 V2 + P2 V1 (fresh accumulator every tile)
+    if (tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t idO = idesc_f16(128, 256, false, true);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {             // 16 cells = 8 TMEM columns of fp16 pairs
+        const uint64_t v1 = smem_desc(sbase + kVfOff + kk * 2048, 8192, 1024);
+        const uint64_t v2 = smem_desc(sbase + kVfOff + 32768 + kk * 2048, 8192, 1024);
+        mma_f16_ta(tmem + kOCol, tmem + kP1Col + 8 * kk, v1, idO, kk > 0 ? 1u : 0u);
+        mma_f16_ta(tmem + kOCol, tmem + kP1Col + 8 * kk, v2, idO, 1u);
+        mma_f16_ta(tmem + kOCol, tmem + kP2Col + 8 * kk, v1, idO, 1u);
+      }
+      mma_commit(bar_o);
+    }
+    if (!mbar_wait(bar_o, phase & 1)) failed = true;
+    tc_fence_after();
+    phase ^= 1;
+    if (__syncthreads_or(failed ? 1 : 0)) { failed = true; break; }
+
+    // ---- merge: o_run = o_run * alpha + O_tile (IEEE fp32 on the CUDA cores)
+    {
+      float o[32];
+      tmem_ld32(tmem + lane_base + kOCol + 64 * part, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o_run[i] = fmaf(o_run[i], alpha, o[i]);
+      tmem_ld32(tmem + lane_base + kOCol + 64 * part + 32, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o_run[32 + i] = fmaf(o_run[32 + i], alpha, o[i]);
+    }
+    tc_fence_before();     // the next tile's MMAs overwrite these columns
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- epilogue: o / l, inverse Walsh-Hadamard transform, write rows
+  if (!failed) {
+    red[part * kRows + row] = l_part;
+    __syncthreads();
+    const float l = (red[row] + red[kRows + row]) + (red[2 * kRows + row] + red[3 * kRows + row]);
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;    // O and l both carry the 2^7 factor of P
+    float* rowbuf = reinterpret_cast<float*>(smem + kKfOff);     // [128][256] fp32, rotated by 4 * row
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      const int d = 64 * part + i;
+      *reinterpret_cast<float4*>(rowbuf + row * 256 + ((d + 4 * row) & 255)) =
+          make_float4(o_run[i] * inv, o_run[i + 1] * inv, o_run[i + 2] * inv, o_run[i + 3] * inv);
+    }
+    __syncthreads();
+    for (int r = warp; r < kRows; r += kThreads / 32) {
+      const int t = tok0 + r / kGqa, h = r % kGqa;
+      if (t >= p.n_q_tok) continue;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; e += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(rowbuf + r * 256 + ((8 * lane + e + 4 * r) & 255));
+        v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
+      }
+#pragma unroll
+      for (int hh = 1; hh < 8; hh <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (e & hh) continue;
+          const float a = v[e], b = v[e + hh];
+          v[e] = a + b;
+          v[e + hh] = a - b;
+        }
+      }
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = __shfl_xor_sync(kFull, v[e], m);
+          v[e] = upper ? x - v[e] : v[e] + x;
+        }
+      }
+      float* dst = p.out + (static_cast<int64_t>(t) * HQ + g * kGqa + h) * kD + 8 * lane;
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0] * 0.0625f, v[1] * 0.0625f, v[2] * 0.0625f, v[3] * 0.0625f);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4] * 0.0625f, v[5] * 0.0625f, v[6] * 0.0625f, v[7] * 0.0625f);
+    }
+  } else {
+    if (tid == 0) {
+      record_status(p.status, K8V4_ECUDA);
+      mma_commit(bar_o);                     // let in-flight MMAs drain (bounded)
+      (void)mbar_wait(bar_o, phase & 1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,
+                   int seq_len, int n_q_tok, const int32_t* steps, float sm_scale, float* out) {
+  if (C.P % kTileN != 0) return K8V4_EINVAL;          // tiles of 64 cells never straddle a page
+  if (n_q_tok == 0) return K8V4_OK;
+  PrefillParams p;
+  p.C = C;
+  p.q = static_cast<const uint16_t*>(q);
+  p.pt = pt;
+  p.max_pages = max_pages;
+  p.steps = steps;
+  p.seq_len = seq_len;
+  p.n_q_tok = n_q_tok;
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.out = out;
+  p.status = L.status;
+  if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return K8V4_ECUDA;
+  const dim3 grid((n_q_tok + kTokens - 1) / kTokens, C.H);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, L.stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
+}
+
 }  // namespace k8v4

@@ -191,6 +191,92 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def measure_verify(args, dev, reps: int = 20):
+    """Config 4: 8 sequences, lengths U[16,384, 65,536], 5 queries each with steps
+    len-4+i, pages interleaved in one pool.  GB/s over 816 B/cell of the cells
+    read (each sequence's longest step)."""
+    import torch
+    import quantized_paged_kv_q8_gb300 as k8
+    import synth
+    w = synth.config4()
+    cache = k8.PagedCache(w.n_pages, w.page_size, w.n_kv, device=dev)
+    pt = torch.from_numpy(w.page_table).to(dev)
+    for b in range(w.n_seqs):
+        n = int(w.seq_lens[b])
+        kd = torch.from_numpy(w.k[b].dev.view(np.int16)).view(torch.bfloat16).reshape(1, n, H, 256).to(dev)
+        vd = torch.from_numpy(w.v[b].dev.view(np.int16)).view(torch.bfloat16).reshape(1, n, H, 256).to(dev)
+        k8.kv_append_k8v4(cache, pt[b:b + 1], torch.zeros(1, dtype=torch.int64, device=dev), kd, vd)
+    q = torch.stack([torch.from_numpy(w.q[b].dev.view(np.int16)).view(torch.bfloat16) for b in range(w.n_seqs)]).to(dev)
+    steps = torch.from_numpy(w.steps).to(dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    max_len = int(w.seq_lens.max())
+    ws = k8.workspace(cache, w.n_seqs, w.n_q, max_len, device=dev)
+    for _ in range(3):
+        k8.attn_k8v4_verify(cache, q, pt, steps, max_len, out, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        k8.attn_k8v4_verify(cache, q, pt, steps, max_len, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    assert k8.k8v4_last_device_status() == 0
+    cells = int(w.seq_lens.sum())
+    return {"workload": "verify_8seq_x5q_U16K-64K", "cells": cells, "ms_per_call": ms,
+            "gbs": CELL_BYTES * cells / (ms / 1e3) / 1e9, "cells_per_s": cells / (ms / 1e3)}
+
+
+def measure_prefill(args, dev, chunk: int, reps: int = 3):
+    """Config 5: 229,376-cell history, then an append of `chunk` tokens at offset
+    229,376 (timed: chunk append cells/s) and causal prefill of the chunk (timed:
+    TFLOP/s over the visible (query, cell) pairs x 16 heads x 1,024 flop)."""
+    import torch
+    import quantized_paged_kv_q8_gb300 as k8
+    import synth
+    w = synth.config5(chunk=chunk)
+    cache = k8.PagedCache(w.n_pages, w.page_size, w.n_kv, device=dev)
+    pt = torch.from_numpy(w.page_table).to(dev)
+
+    def kv(lo, n):
+        k, v = synth.prefill_kv(w, lo, n)
+        return (torch.from_numpy(k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, n, H, 256).to(dev),
+                torch.from_numpy(v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, n, H, 256).to(dev))
+    hk, hv = kv(0, w.history)
+    k8.kv_append_k8v4(cache, pt, torch.zeros(1, dtype=torch.int64, device=dev), hk, hv)
+    del hk, hv
+    ck, cv = kv(w.history, w.chunk)
+    off = torch.full((1,), w.history, dtype=torch.int64, device=dev)
+    k8.kv_append_k8v4(cache, pt, off, ck, cv)
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(10):
+        k8.kv_append_k8v4(cache, pt, off, ck, cv)
+    a1.record()
+    torch.cuda.synchronize()
+    app_ms = a0.elapsed_time(a1) / 10
+    q = synth.prefill_q(w)
+    qd = torch.from_numpy(q.dev.view(np.int16)).view(torch.bfloat16).reshape(w.chunk, HQ, 256).to(dev)
+    out = torch.empty(w.chunk, HQ, 256, dtype=torch.float32, device=dev)
+    k8.attn_k8v4_prefill(cache, qd, pt[0], w.total, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        k8.attn_k8v4_prefill(cache, qd, pt[0], w.total, out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    assert k8.k8v4_last_device_status() == 0
+    pairs = sum(w.history + t + 1 for t in range(w.chunk))
+    flop = pairs * HQ * 1024
+    return {"workload": f"prefill_{w.chunk}_tokens_at_{w.history}", "ms_per_call": ms, "tflop": flop / 1e12,
+            "tflops": flop / (ms / 1e3) / 1e12,
+            "chunk_append": {"cells": w.chunk, "ms": app_ms, "cells_per_s": w.chunk / (app_ms / 1e3),
+                             "gbs": APPEND_BYTES * w.chunk / (app_ms / 1e3) / 1e9}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -198,8 +284,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="k8v4", choices=["k8v4", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", action="store_true",
-                    help="lean run for ncu: one cache replica, no INT8 arm / e2e / CPU baseline")
+    ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify"],
+                    help="lean single-kernel run for ncu (no replicas, INT8 arm, e2e or CPU baseline)")
+    ap.add_argument("--chunk", type=int, default=8192, help="prefill chunk length (tokens)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -219,6 +306,12 @@ def main():
     from quantized_paged_kv_q8_gb300 import buildlib
     buildlib.build()
     assert k8.k8v4_device_check() == 0, "libk8v4 needs an sm_103 device"
+
+    if args.profile in ("prefill", "verify"):
+        res = measure_prefill(args, dev, args.chunk) if args.profile == "prefill" else measure_verify(args, dev)
+        if rank == 0:
+            print(json.dumps({"profile": args.profile, **res}), flush=True)
+        return
 
     w = synth.config3(N_CELLS)
     n_pages = w.n_pages
@@ -347,7 +440,12 @@ def main():
     h2d = q.numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2
     d2h = out.numel() * 4
 
-    hbm, bf16, _, peak_kind = peaks()
+    del caches, kd, vd
+    torch.cuda.empty_cache()
+    verify = measure_verify(args, dev)
+    prefill = measure_prefill(args, dev, 8192)
+
+    hbm, bf16, bf16_sus, peak_kind = peaks()
     dec_bytes = CELL_BYTES * N_CELLS
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
     traffic = traffic_record("attend_splitk_decode_237568")
@@ -373,6 +471,11 @@ def main():
                      "k8v4_speedup": int8_ms / dec_ms},
         "e2e": {"value": dec_bytes / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "verify": {**verify, "frac_hbm": verify["gbs"] / hbm},
+        "prefill": {**prefill, "frac_bf16_burst": prefill["tflops"] / bf16,
+                    "frac_bf16_sustained": prefill["tflops"] / bf16_sus,
+                    "peak_note": "bf16 dense cuBLAS peaks from MEASURED_PEAKS.json (burst and sustained); the "
+                                 "kernel's fp16 operands run at the same nominal rate"},
         "gpu_launches": 3 * K,
         "clocks": clk.summary(),
     }

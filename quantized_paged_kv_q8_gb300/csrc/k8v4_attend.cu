@@ -32,6 +32,9 @@ constexpr unsigned kFull = 0xffffffffu;
 #ifndef K8V4_STAGES
 #define K8V4_STAGES 3
 #endif
+#ifndef K8V4_QF_SMEM
+#define K8V4_QF_SMEM 0       // 1: q fragments live in shared memory instead of registers
+#endif
 #ifndef K8V4_DECODE_WARPS
 #define K8V4_DECODE_WARPS 8
 #endif
@@ -128,47 +131,55 @@ __device__ __forceinline__ uint32_t i8_to_bf16(uint32_t r, uint32_t s0, uint32_t
 }
 
 // ---------------------------------------------------------------- tile loader
-template <int FMT>
-__device__ __forceinline__ void load_tile(const AttendParams& p, uint8_t* stage, const uint8_t* base, int slot0,
-                                          int g, int tid, int nthr) {
-  const CacheView& C = p.C;
-  const uint32_t s = smem_u32(stage);
+// Stage one 16-cell tile of KV head g (cells slot0 .. slot0+15 of one page) with
+// 16-byte cp.async copies.  NTHR > 0 fixes the group size at compile time (the
+// loops then unroll); NTHR == 0 reads it from nthr.
+template <int FMT, int NTHR>
+__device__ __forceinline__ void load_tile(const CacheView& C, uint32_t s, const uint8_t* base, int slot0, int g,
+                                          int tid, int nthr_rt) {
+  const int nthr = NTHR > 0 ? NTHR : nthr_rt;
   const int H = C.H;
+  const int64_t r0 = static_cast<int64_t>(slot0) * H + g;       // (cell, head) index of the tile's first row
+  const uint8_t* kb = base + r0 * 256;
+  const uint8_t* vb = base + C.v_off() + r0 * C.v_row_bytes();
+  const uint8_t* ksb = base + C.ks_off() + r0 * 8;
+  const uint8_t* vsb = base + C.vs_off() + r0 * C.vs_row_bytes();
+  const int kst = H * 256, vst = H * C.v_row_bytes();
   // K codes: 16 cells x 16 chunks; chunk kk of cell j stored at kk ^ (4 * (j & 1))
+#pragma unroll
   for (int i = tid; i < 256; i += nthr) {
     const int j = i >> 4, kk = i & 15;
-    const uint8_t* src = base + (static_cast<int64_t>(slot0 + j) * H + g) * 256 + 16 * kk;
-    cp_async16(s + Stage<FMT>::kK + j * 256 + 16 * (kk ^ ((j & 1) << 2)), src);
+    cp_async16(s + Stage<FMT>::kK + j * 256 + 16 * (kk ^ ((j & 1) << 2)), kb + j * kst + 16 * kk);
   }
   if (FMT == K8V4_FORMAT_K8V4) {
     // V nibbles: 16 cells x 8 blocks; block b of cell j stored at b ^ (j & 7)
+#pragma unroll
     for (int i = tid; i < 128; i += nthr) {
       const int j = i >> 3, bb = i & 7;
-      const uint8_t* src = base + C.v_off() + (static_cast<int64_t>(slot0 + j) * H + g) * 128 + 16 * bb;
-      cp_async16(s + Stage<FMT>::kV + j * 128 + 16 * (bb ^ (j & 7)), src);
+      cp_async16(s + Stage<FMT>::kV + j * 128 + 16 * (bb ^ (j & 7)), vb + j * vst + 16 * bb);
     }
   } else {
+#pragma unroll
     for (int i = tid; i < 256; i += nthr) {
       const int j = i >> 4, kk = i & 15;
-      const uint8_t* src = base + C.v_off() + (static_cast<int64_t>(slot0 + j) * H + g) * 256 + 16 * kk;
-      cp_async16(s + Stage<FMT>::kV + j * 256 + 16 * (kk ^ (j & 7)), src);
+      cp_async16(s + Stage<FMT>::kV + j * 256 + 16 * (kk ^ (j & 7)), vb + j * vst + 16 * kk);
     }
   }
+#pragma unroll
   for (int i = tid; i < 32; i += nthr) {
     const int j = i & 15;
-    const int64_t r = static_cast<int64_t>(slot0 + j) * H + g;
     if (i < 16) {
-      cp_async8(s + Stage<FMT>::kKs + 8 * j, base + C.ks_off() + r * 8);
+      cp_async8(s + Stage<FMT>::kKs + 8 * j, ksb + j * (H * 8));
     } else if (FMT == K8V4_FORMAT_K8V4) {
-      cp_async16(s + Stage<FMT>::kVs + 16 * j, base + C.vs_off() + r * 16);
+      cp_async16(s + Stage<FMT>::kVs + 16 * j, vsb + j * (H * 16));
     } else {
-      cp_async8(s + Stage<FMT>::kVs + 8 * j, base + C.vs_off() + r * 8);
+      cp_async8(s + Stage<FMT>::kVs + 8 * j, vsb + j * (H * 8));
     }
   }
 }
 
 // ---------------------------------------------------------------- main kernel
-template <int FMT, bool QF32>
+template <int FMT, bool QF32, bool NQ1>
 __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const AttendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   using S = Stage<FMT>;
@@ -258,6 +269,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
       }
     }
   }
+#if K8V4_QF_SMEM
+  // per-warp q fragments after the tile-group stages: [8 pairs of k-steps][32 lanes] x 16 B
+  uint4* qsm = reinterpret_cast<uint4*>(smem + static_cast<size_t>(p.n_groups) * kStages * S::kBytes) + warp * 8 * 32;
+#pragma unroll
+  for (int kp = 0; kp < 8; ++kp)
+    qsm[kp * 32 + lane] = make_uint4(qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+  __syncwarp();
+#endif
   // score factors for the heads of the C layout (2c, 2c+1): held by lanes 4h
   const float f0 = __shfl_sync(kFull, fscale, 8 * c), f1 = __shfl_sync(kFull, fscale, 8 * c + 4);
 
@@ -268,47 +287,51 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
 
   // ---- pipeline over this group's tiles: gi, gi + n_groups, ...
   uint8_t* gbuf = smem + static_cast<size_t>(gi) * kStages * S::kBytes;
+  const uint32_t gbuf_s = smem_u32(gbuf);
   const int n_my = n_tiles > gi ? (n_tiles - gi + p.n_groups - 1) / p.n_groups : 0;
-  const int tid = qi * 32 + lane, nthr = p.n_q * 32;
-  auto tile_page = [&](int t, int& slot0) -> const uint8_t* {
-    const int cell0 = c_begin + 16 * (gi + t * p.n_groups);
-    const int64_t pidx = cell0 / C.P;
-    slot0 = cell0 % C.P;
-    if (pidx >= p.max_pages) return nullptr;
-    const int64_t page = p.pt[static_cast<int64_t>(b) * p.max_pages + pidx];
-    if (page < 0 || page >= C.n_pages) return nullptr;
-    return C.pages + page * C.page_bytes;
+  const int tid = qi * 32 + lane, nthr = NQ1 ? 32 : p.n_q * 32;
+  // load cursor: page index and slot of the next tile to stage (advanced, never divided again)
+  const int step = 16 * p.n_groups;
+  int64_t lp = 0;
+  int ls = 0;
+  {
+    const int cell = c_begin + 16 * gi;
+    lp = cell / C.P;
+    ls = cell - static_cast<int>(lp) * C.P;
+  }
+  const int32_t* pt_row = p.pt + static_cast<int64_t>(b) * p.max_pages;
+  uint32_t vmask = 0;                          // bit s: stage s holds a valid tile
+  auto issue = [&](int stage) {
+    const int64_t page = lp < p.max_pages ? pt_row[lp] : -1;
+    if (page >= 0 && page < C.n_pages) {
+      load_tile<FMT, NQ1 ? 32 : 0>(C, gbuf_s + stage * S::kBytes, C.pages + page * C.page_bytes, ls, g, tid, nthr);
+      vmask |= 1u << stage;
+    } else {
+      vmask &= ~(1u << stage);
+      if (tid == 0) record_status(p.status, K8V4_ERANGE);
+    }
+    ls += step;
+    while (ls >= C.P) { ls -= C.P; ++lp; }
   };
 #pragma unroll 1
   for (int s = 0; s < kStages - 1; ++s) {
-    if (s < n_my) {
-      int slot0;
-      const uint8_t* base = tile_page(s, slot0);
-      if (base) load_tile<FMT>(p, gbuf + s * S::kBytes, base, slot0, g, tid, nthr);
-      else if (tid == 0) record_status(p.status, K8V4_ERANGE);
-    }
+    if (s < n_my) issue(s);
     cp_async_commit();
   }
 #pragma unroll 1
   for (int it = 0; it < n_my; ++it) {
+    const int cur = it % kStages;
     cp_async_wait<kStages - 2>();
-    if (nthr == 32) __syncwarp();          // a one-warp group needs no CTA barrier
+    if (NQ1 || nthr == 32) __syncwarp();   // a one-warp group needs no CTA barrier
     else named_barrier(1 + gi, nthr);
     {
       const int nx = it + kStages - 1;
-      if (nx < n_my) {
-        int slot0;
-        const uint8_t* base = tile_page(nx, slot0);
-        if (base) load_tile<FMT>(p, gbuf + (nx % kStages) * S::kBytes, base, slot0, g, tid, nthr);
-        else if (tid == 0) record_status(p.status, K8V4_ERANGE);
-      }
+      if (nx < n_my) issue(nx % kStages);
       cp_async_commit();
     }
-    int slot_unused;
-    const bool valid = tile_page(it, slot_unused) != nullptr;
     const int cell0 = c_begin + 16 * (gi + it * p.n_groups);
-    if (!valid || cell0 >= lim) continue;      // nothing visible for this query
-    const uint8_t* st = gbuf + (it % kStages) * S::kBytes;
+    if (!((vmask >> cur) & 1u) || cell0 >= lim) continue;      // nothing visible for this query
+    const uint8_t* st = gbuf + cur * S::kBytes;
     const uint32_t st_s = smem_u32(st);
 
     // ---- QK^T: S^T[cell][head], halves accumulated separately; two
@@ -327,10 +350,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
         codes_to_f16(wa[j], a[j][0], a[j][2]);
         codes_to_f16(wb[j], a[j][1], a[j][3]);
       }
+#if K8V4_QF_SMEM
+      const uint4 qa = qsm[(2 * i) * 32 + lane], qb = qsm[(2 * i + 1) * 32 + lane];
+      const uint32_t qq[4][2] = {{qa.x, qa.y}, {qa.z, qa.w}, {qb.x, qb.y}, {qb.z, qb.w}};
+#endif
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float* dst = acc[2 * (i >> 1) + (j & 1)];
+#if K8V4_QF_SMEM
+        mma_f16(dst, a[j], qq[j][0], qq[j][1]);
+#else
         mma_f16(dst, a[j], qf[4 * i + j][0], qf[4 * i + j][1]);
+#endif
         if (QF32) mma_f16(dst, a[j], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][0], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][1]);
       }
     }
@@ -387,6 +418,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
       P[3] = __uint_as_float(prmt(tl1, th1, 0x7632u));
     }
     const int pc[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    const float2 P01 = make_float2(P[0], P[1]), P23 = make_float2(P[2], P[3]);
 
     // ---- PV in rotated space
     if (FMT == K8V4_FORMAT_K8V4) {
@@ -404,20 +436,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int bl = bp + h;
-          float x[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t word = (bl >> 1) == 0 ? dv[t].x : (bl >> 1) == 1 ? dv[t].y : (bl >> 1) == 2 ? dv[t].z : dv[t].w;
-            const __half dh = __ushort_as_half(static_cast<unsigned short>((bl & 1) ? (word >> 16) : (word & 0xffffu)));
-            x[t] = P[t] * __half2float(dh);
-          }
+          // d of block bl for cells (2c, 2c+1) and (2c+8, 2c+9), as fp16 pairs
+          const uint32_t sel = (bl & 1) ? 0x7632u : 0x5410u;
+          const uint32_t wA = (bl >> 1) == 0 ? dv[0].x : (bl >> 1) == 1 ? dv[0].y : (bl >> 1) == 2 ? dv[0].z : dv[0].w;
+          const uint32_t wB = (bl >> 1) == 0 ? dv[1].x : (bl >> 1) == 1 ? dv[1].y : (bl >> 1) == 2 ? dv[1].z : dv[1].w;
+          const uint32_t wC = (bl >> 1) == 0 ? dv[2].x : (bl >> 1) == 1 ? dv[2].y : (bl >> 1) == 2 ? dv[2].z : dv[2].w;
+          const uint32_t wD = (bl >> 1) == 0 ? dv[3].x : (bl >> 1) == 1 ? dv[3].y : (bl >> 1) == 2 ? dv[3].z : dv[3].w;
+          uint32_t d01 = prmt(wA, wB, sel), d23 = prmt(wC, wD, sel);
+          float2 x01 = __fmul2_rn(P01, __half22float2(*reinterpret_cast<__half2*>(&d01)));
+          float2 x23 = __fmul2_rn(P23, __half22float2(*reinterpret_cast<__half2*>(&d23)));
 #pragma unroll
           for (int pl = 0; pl < kPlanes; ++pl) {
-            B[h][pl][0] = pack_bf16(x[0], x[1]);
-            B[h][pl][1] = pack_bf16(x[2], x[3]);
-            if (pl + 1 < kPlanes) {
-              x[0] -= bf16_lo(B[h][pl][0]); x[1] -= bf16_hi(B[h][pl][0]);
-              x[2] -= bf16_lo(B[h][pl][1]); x[3] -= bf16_hi(B[h][pl][1]);
+            B[h][pl][0] = pack_bf16(x01.x, x01.y);
+            B[h][pl][1] = pack_bf16(x23.x, x23.y);
+            if (pl + 1 < kPlanes) {   // exact residuals: x - bf16(x)
+              x01 = __ffma2_rn(make_float2(bf16_lo(B[h][pl][0]), bf16_hi(B[h][pl][0])), make_float2(-1.0f, -1.0f), x01);
+              x23 = __ffma2_rn(make_float2(bf16_lo(B[h][pl][1]), bf16_hi(B[h][pl][1])), make_float2(-1.0f, -1.0f), x23);
             }
           }
           const uint32_t Ra = R[2 * h], Rb = R[2 * h + 1];
@@ -504,131 +538,158 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     mine[2056 + 2 * c + 1] = l1;
   }
   __syncthreads();
-  const int total = p.n_q * 8 * 256;
-  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-    const int q2 = idx >> 11, h = (idx >> 8) & 7, dim = idx & 255;
+  // one warp per output row (query, head): merge the tile groups, bring the
+  // partial back from rotated space (out = (H/16) o is linear, so the split
+  // combine can work on un-rotated partials) and write (o, m, l)
+  const int n_rows = p.n_q * kGqa;
+  for (int rr = warp; rr < n_rows; rr += blockDim.x >> 5) {
+    const int q2 = rr >> 3, h = rr & 7;
     float M = -INFINITY;
     for (int gg = 0; gg < p.n_groups; ++gg) M = fmaxf(M, mo[static_cast<size_t>(gg * p.n_q + q2) * kWS + 2048 + h]);
-    float acc = 0.0f, L = 0.0f;
+    float v[8], L = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
     if (M != -INFINITY) {
       for (int gg = 0; gg < p.n_groups; ++gg) {
         const float* src = mo + static_cast<size_t>(gg * p.n_q + q2) * kWS;
         const float mg = src[2048 + h];
         if (mg == -INFINITY) continue;
         const float sc2 = exp2f(mg - M);
-        acc += src[h * 256 + dim] * sc2;
+        const float4 x0 = *reinterpret_cast<const float4*>(src + h * 256 + 8 * lane);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + h * 256 + 8 * lane + 4);
+        v[0] += x0.x * sc2; v[1] += x0.y * sc2; v[2] += x0.z * sc2; v[3] += x0.w * sc2;
+        v[4] += x1.x * sc2; v[5] += x1.y * sc2; v[6] += x1.z * sc2; v[7] += x1.w * sc2;
         L += src[2056 + h] * sc2;
       }
     }
+    if (FMT == K8V4_FORMAT_K8V4) {
+#pragma unroll
+      for (int hh = 1; hh < 8; hh <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (e & hh) continue;
+          const float a = v[e], bb = v[e + hh];
+          v[e] = a + bb;
+          v[e + hh] = a - bb;
+        }
+      }
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = __shfl_xor_sync(kFull, v[e], m);
+          v[e] = upper ? t - v[e] : v[e] + t;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] *= 0.0625f;
+    }
     float* dst = p.ws + ((((static_cast<int64_t>(b) * p.splits + split) * p.n_q + q2) * HQ) + g * kGqa + h) * kPStride;
-    dst[dim] = acc;
-    if (dim == 0) {
+    reinterpret_cast<float4*>(dst + 8 * lane)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst + 8 * lane)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    if (lane == 0) {
       dst[256] = M;
       dst[257] = L;
     }
   }
+  // the combine kernel may start once every partial of this grid is written
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per output row (b, query, head); thread t owns rotated dim t.  The
-// split maxima are reduced first, then every thread sums its dim over the
-// splits with independent loads; one warp applies the inverse transform.
-template <int FMT>
+// Weighted sum of the splits' (already un-rotated) partials.  One CTA per
+// (output row, 32-dim chunk): the split maxima and weights are reduced first,
+// then warp w sums splits w, w+8, ... for its lane's dim with independent loads,
+// and the eight warp sums are added in shared memory.  Launched as a
+// programmatic dependent of the split kernel (griddepcontrol.wait).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws, int splits, int n_q, int HQ,
                                                       float* __restrict__ out) {
-  __shared__ float red[256];
-  __shared__ float mx[8];
+  constexpr int kMaxSplitsInSmem = 1024;
+  __shared__ float wgt[kMaxSplitsInSmem];
+  __shared__ float red[8][33];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int row = blockIdx.x;                 // (b, qi, head)
+  const int row = blockIdx.x, chunk = blockIdx.y;   // row = (b, qi, head)
   const int head = row % HQ;
-  const int bq = row / HQ;                    // b * n_q + qi
+  const int bq = row / HQ;
   const int b = bq / n_q, qi = bq % n_q;
-  const int64_t stride = static_cast<int64_t>(n_q) * HQ * kPStride;    // between splits
+  const int64_t stride = static_cast<int64_t>(n_q) * HQ * kPStride;     // between splits
   const float* base = ws + ((static_cast<int64_t>(b) * splits * n_q + qi) * HQ + head) * kPStride;
+  // pass 1: M = max_s m_s
   float M = -INFINITY;
   for (int s = t; s < splits; s += 256) M = fmaxf(M, base[s * stride + 256]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  if (lane == 0) mx[warp] = M;
+  if (lane == 0) red[warp][32] = M;
   __syncthreads();
-  M = mx[0];
+  M = red[0][32];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, mx[w]);
-  float acc = 0.0f, L = 0.0f;
-  if (M != -INFINITY) {
-    int s = 0;
-    for (; s + 4 <= splits; s += 4) {
-      float ms[4], ls[4], xs[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float* src = base + (s + u) * stride;
-        ms[u] = src[256];
-        ls[u] = src[257];
-        xs[u] = src[t];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float wgt = ms[u] == -INFINITY ? 0.0f : exp2f(ms[u] - M);
-        acc += xs[u] * wgt;
-        L += ls[u] * wgt;
-      }
-    }
-    for (; s < splits; ++s) {
-      const float* src = base + s * stride;
-      const float ms = src[256];
-      const float wgt = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-      acc += src[t] * wgt;
-      L += src[257] * wgt;
-    }
-  }
-  red[t] = L > 0.0f ? acc / L : 0.0f;
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w][32]);
   __syncthreads();
-  if (warp != 0) return;
-  float v[8];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) v[r] = red[8 * lane + r];
-  if (FMT == K8V4_FORMAT_K8V4) {
-    // out = (H/16) o: fast Walsh-Hadamard transform over element 8 * lane + r
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if (r & h) continue;
-        const float a = v[r], bb = v[r + h];
-        v[r] = a + bb;
-        v[r + h] = a - bb;
-      }
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const bool upper = (lane & m) != 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float tt = __shfl_xor_sync(kFull, v[r], m);
-        v[r] = upper ? tt - v[r] : v[r] + tt;
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 8; ++r) v[r] *= 0.0625f;
+  // weights w_s = exp2(m_s - M) and L = sum_s l_s w_s
+  float L = 0.0f;
+  for (int s = t; s < splits; s += 256) {
+    const float ms = base[s * stride + 256];
+    const float w = (M == -INFINITY || ms == -INFINITY) ? 0.0f : exp2f(ms - M);
+    if (s < kMaxSplitsInSmem) wgt[s] = w;
+    L += base[s * stride + 257] * w;
   }
-  float* dst = out + static_cast<int64_t>(row) * kD + 8 * lane;
-  reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+  if (lane == 0) red[warp][32] = L;
+  __syncthreads();
+  L = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) L += red[w][32];
+  // pass 2: sum of weighted partials for dim chunk*32 + lane
+  const int dim = chunk * 32 + lane;
+  float acc = 0.0f;
+#pragma unroll 4
+  for (int s = warp; s < splits; s += 8) {
+    const float w = s < kMaxSplitsInSmem ? wgt[s] : ((M == -INFINITY || base[s * stride + 256] == -INFINITY)
+                                                          ? 0.0f : exp2f(base[s * stride + 256] - M));
+    acc += base[s * stride + dim] * w;
+  }
+  red[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += red[w][lane];
+    out[static_cast<int64_t>(row) * kD + dim] = L > 0.0f ? v / L : 0.0f;
+  }
 }
 
-template <int FMT, bool QF32>
+template <int FMT, bool QF32, bool NQ1>
 int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, float* out) {
-  const size_t stage_bytes = static_cast<size_t>(plan.n_groups) * kStages * Stage<FMT>::kBytes;
+  const size_t stage_bytes = static_cast<size_t>(plan.n_groups) * kStages * Stage<FMT>::kBytes +
+                             (K8V4_QF_SMEM ? static_cast<size_t>(plan.warps) * 8 * 32 * 16 : 0);
   const size_t merge_bytes = static_cast<size_t>(plan.warps) * (8 * 256 + 16) * sizeof(float);
   const size_t smem = stage_bytes > merge_bytes ? stage_bytes : merge_bytes;
-  auto kern = attend_splitk_kernel<FMT, QF32>;
+  auto kern = attend_splitk_kernel<FMT, QF32, NQ1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return K8V4_ECUDA;
   const dim3 grid(plan.splits, p.C.H, p.n_seqs);
   kern<<<grid, plan.warps * 32, smem, L.stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
+  // combine: a programmatic dependent launch, so its launch overlaps the tail
+  // of the split kernel; it waits (griddepcontrol.wait) for the partials
   const int rows = p.n_seqs * p.n_q * p.C.H * kGqa;
-  combine_kernel<FMT><<<rows, 256, 0, L.stream>>>(p.ws, plan.splits, p.n_q, p.C.H * kGqa, out);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows, kD / 32);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(p.ws), plan.splits, p.n_q,
+                         p.C.H * kGqa, out) != cudaSuccess)
+    return K8V4_ECUDA;
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
 }
 
@@ -675,10 +736,17 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.ws = static_cast<float*>(ws);
   p.status = L.status;
-  const bool f32 = q_dtype == K8V4_F32;
-  if (C.fmt == K8V4_FORMAT_K8V4)
-    return f32 ? launch_impl<K8V4_FORMAT_K8V4, true>(L, p, plan, out) : launch_impl<K8V4_FORMAT_K8V4, false>(L, p, plan, out);
-  return f32 ? launch_impl<K8V4_FORMAT_INT8, true>(L, p, plan, out) : launch_impl<K8V4_FORMAT_INT8, false>(L, p, plan, out);
+  const bool f32 = q_dtype == K8V4_F32, one = plan.n_q == 1;
+  if (C.fmt == K8V4_FORMAT_K8V4) {
+    if (f32) return one ? launch_impl<K8V4_FORMAT_K8V4, true, true>(L, p, plan, out)
+                        : launch_impl<K8V4_FORMAT_K8V4, true, false>(L, p, plan, out);
+    return one ? launch_impl<K8V4_FORMAT_K8V4, false, true>(L, p, plan, out)
+               : launch_impl<K8V4_FORMAT_K8V4, false, false>(L, p, plan, out);
+  }
+  if (f32) return one ? launch_impl<K8V4_FORMAT_INT8, true, true>(L, p, plan, out)
+                      : launch_impl<K8V4_FORMAT_INT8, true, false>(L, p, plan, out);
+  return one ? launch_impl<K8V4_FORMAT_INT8, false, true>(L, p, plan, out)
+             : launch_impl<K8V4_FORMAT_INT8, false, false>(L, p, plan, out);
 }
 
 }  // namespace k8v4

@@ -301,8 +301,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
   }
   const int32_t* pt_row = p.pt + static_cast<int64_t>(b) * p.max_pages;
   uint32_t vmask = 0;                          // bit s: stage s holds a valid tile
+  // the page id of the next tile to stage is read one issue ahead, so the
+  // global-load latency hides behind a tile of compute
+  int64_t nxt_page = (n_my > 0 && lp < p.max_pages) ? pt_row[lp] : -1;
   auto issue = [&](int stage) {
-    const int64_t page = lp < p.max_pages ? pt_row[lp] : -1;
+    const int64_t page = nxt_page;
     if (page >= 0 && page < C.n_pages) {
       load_tile<FMT, NQ1 ? 32 : 0>(C, gbuf_s + stage * S::kBytes, C.pages + page * C.page_bytes, ls, g, tid, nthr);
       vmask |= 1u << stage;
@@ -312,6 +315,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     }
     ls += step;
     while (ls >= C.P) { ls -= C.P; ++lp; }
+    nxt_page = lp < p.max_pages ? pt_row[lp] : -1;
   };
 #pragma unroll 1
   for (int s = 0; s < kStages - 1; ++s) {

@@ -63,9 +63,9 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // the epilogue reuses [kKfOff, kKfOff + 128 KB) as a fp32 [128][256] row buffer
 static_assert(kBarOff - kKfOff >= 128 * 256 * 4, "epilogue buffer");
 
-constexpr uint32_t kTmemCols = 512;    // S0 [0,64), S1 [64,128), O_tile [128,384); P1/P2 reuse [0,64)
-constexpr uint32_t kS0Col = 0, kS1Col = 64, kOCol = 128, kP1Col = 0, kP2Col = 32;
-constexpr float kPScale = 128.0f;      // P is stored as p * 2^7 (p <= 1 -> <= 2^7; keeps tiny p normal in fp16)
+constexpr uint32_t kTmemCols = 512;    // S buffers [0,128) and [128,256) (S0 | S1 each; P1/P2 reuse
+                                       // the buffer's S0 columns), O_tile [256,512)
+constexpr uint32_t kSBuf = 128, kS0Col = 0, kS1Col = 64, kOCol = 256, kP1Col = 0, kP2Col = 32;
 constexpr uint32_t kSpinLimit = 1u << 22;     // ~1 s of try_wait polling
 
 struct PrefillParams {
@@ -184,24 +184,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float v[8]) {
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float v[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -252,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   const CacheView& C = p.C;
   const int HQ = C.H * kGqa;
 
-  const uint32_t bar_s = sbase + kBarOff, bar_o = sbase + kBarOff + 8;
+  const uint32_t bar_s = sbase + kBarOff, bar_o = sbase + kBarOff + 8, bar_d = sbase + kBarOff + 32;
   const uint32_t tmem_slot = sbase + kBarOff + 16;
   int* nmax_s = reinterpret_cast<int*>(smem + kBarOff + 28);
   float* red = reinterpret_cast<float*>(smem + kRedOff);           // [4][128] partial maxima / sums
@@ -274,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   if (tid == 0) {
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
+    mbar_init(bar_d, 1);
     *nmax_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -337,22 +320,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
   // ---- raw tile loader (all threads, 16-byte cp.async)
+  // page ids are read one load ahead (tiles are staged in order 0, 1, 2, ...)
+  auto fetch_page = [&](int tile) -> int64_t {
+    const int64_t pidx = static_cast<int64_t>(tile) * kTileN / C.P;
+    return (tile < n_tiles && pidx < p.max_pages) ? static_cast<int64_t>(p.pt[pidx]) : -1;
+  };
+  int64_t pf_page = fetch_page(0);
   auto load_raw = [&](int tile, int stage) {
     const int cell0 = tile * kTileN;
-    const int64_t pidx = cell0 / C.P;
     const uint32_t dst = sbase + kRawOff + stage * kRawBytes;
-    if (pidx >= p.max_pages) return false;
-    const int64_t page = p.pt[pidx];
+    const int64_t page = pf_page;
+    pf_page = fetch_page(tile + 1);
     if (page < 0 || page >= C.n_pages) return false;
     const int slot0 = cell0 % C.P;       // P is a multiple of 64 here
     const uint8_t* base = C.pages + page * C.page_bytes;
+    // raw K chunk kk of cell j sits at 16 * (kk ^ (j & 15)), raw V block b of cell
+    // j at 16 * (b ^ (j & 7)): eight consecutive cells then hit eight different
+    // bank groups when the converters read one chunk of each
     for (int i = tid; i < 64 * 16; i += kThreads) {              // K codes
       const int j = i >> 4, kk = i & 15;
-      cp_async16(dst + j * 256 + 16 * kk, base + (static_cast<int64_t>(slot0 + j) * C.H + g) * 256 + 16 * kk);
+      cp_async16(dst + j * 256 + 16 * (kk ^ (j & 15)), base + (static_cast<int64_t>(slot0 + j) * C.H + g) * 256 + 16 * kk);
     }
     {                                                            // V nibbles: 64 cells x 8 blocks
       const int j = tid >> 3, kk = tid & 7;
-      cp_async16(dst + kRawK + j * 128 + 16 * kk,
+      cp_async16(dst + kRawK + j * 128 + 16 * (kk ^ (j & 7)),
                  base + C.v_off() + (static_cast<int64_t>(slot0 + j) * C.H + g) * 128 + 16 * kk);
     }
     if (tid < 64) {
@@ -363,6 +354,92 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     return true;
   };
 
+  // ---- dequantisation of one raw stage into the operand tiles
+  auto convert_k = [&](int stage) {                 // K codes -> Kf (fp16, exact), K scales -> ks buffer
+    const uint32_t raw = sbase + kRawOff + stage * kRawBytes;
+    for (int i = tid; i < 64 * 16; i += kThreads) {  // (cell j, 16-byte chunk kk); j fastest so a
+      const int j = i & 63, kk = i >> 6;              // quarter-warp covers 8 cells of one chunk
+      const uint4 w = lds128(raw + j * 256 + 16 * (kk ^ (j & 15)));
+      uint32_t h[8];
+      i8x4_to_f16(w.x, h[0], h[1]);
+      i8x4_to_f16(w.y, h[2], h[3]);
+      i8x4_to_f16(w.z, h[4], h[5]);
+      i8x4_to_f16(w.w, h[6], h[7]);
+      const int dim = 16 * kk, chunk = dim >> 6, unit = (dim & 63) >> 3;
+      const uint32_t dst = sbase + kKfOff + chunk * 8192;
+      sts128(dst + swz(j, unit), h[0], h[1], h[2], h[3]);
+      sts128(dst + swz(j, unit + 1), h[4], h[5], h[6], h[7]);
+    }
+    if (tid < 64)
+      reinterpret_cast<float2*>(smem + kKsBufOff)[tid] =
+          reinterpret_cast<const float2*>(smem + kRawOff + stage * kRawBytes + kRawK + kRawV)[tid];
+  };
+  auto convert_v = [&](int stage) {                 // V nibbles x d -> Vf planes (fp16, exact split)
+    const uint32_t raw = sbase + kRawOff + stage * kRawBytes;
+    const int j = tid & 63, b = tid >> 6;           // (cell j, block b): one item per thread, j fastest
+    const uint4 w = lds128(raw + kRawK + j * 128 + 16 * (b ^ (j & 7)));
+    const __half dh = *reinterpret_cast<const __half*>(smem + kRawOff + stage * kRawBytes + kRawK + kRawV +
+                                                          kRawKs + 16 * j + 2 * b);
+    const __half2 d2 = __halves2half2(dh, dh);
+    const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+    uint32_t lo[2][8], hi[2][8];   // [plane] dims 32b + (0..15) and 32b + 16 + (0..15), 8 pairs each
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t t01 = prmt(ws4[q], 0u, 0x5140u);   // {b0, 0, b1, 0}
+      const uint32_t t23 = prmt(ws4[q], 0u, 0x5342u);   // {b2, 0, b3, 0}
+      nib_vhat(t01, 0, d2, lo[0][2 * q], lo[1][2 * q]);
+      nib_vhat(t23, 0, d2, lo[0][2 * q + 1], lo[1][2 * q + 1]);
+      nib_vhat(t01, 4, d2, hi[0][2 * q], hi[1][2 * q]);
+      nib_vhat(t23, 4, d2, hi[0][2 * q + 1], hi[1][2 * q + 1]);
+    }
+    const int atom = b >> 1, unit0 = 4 * (b & 1);
+#pragma unroll
+    for (int pl = 0; pl < 2; ++pl) {
+      const uint32_t dst = sbase + kVfOff + pl * 32768 + atom * 8192;
+      sts128(dst + swz(j, unit0), lo[pl][0], lo[pl][1], lo[pl][2], lo[pl][3]);
+      sts128(dst + swz(j, unit0 + 1), lo[pl][4], lo[pl][5], lo[pl][6], lo[pl][7]);
+      sts128(dst + swz(j, unit0 + 2), hi[pl][0], hi[pl][1], hi[pl][2], hi[pl][3]);
+      sts128(dst + swz(j, unit0 + 3), hi[pl][4], hi[pl][5], hi[pl][6], hi[pl][7]);
+    }
+  };
+  // ---- tensor-core work (one thread issues)
+  auto issue_qk = [&](int buf) {                  // S[buf]_h = Q_h Kf_h^T, fresh accumulators
+    tc_fence_after();
+    constexpr uint32_t idS = idesc_f16(128, 64, false, false);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int chunk = 2 * h + (kk >> 2);
+        const uint32_t off = (kk & 3) * 32;
+        const uint64_t a = smem_desc(sbase + kQOff + chunk * 16384 + off, 16, 1024);
+        const uint64_t b = smem_desc(sbase + kKfOff + chunk * 8192 + off, 16, 1024);
+        mma_f16(tmem + kSBuf * buf + (h ? kS1Col : kS0Col), a, b, idS, kk > 0 ? 1u : 0u);
+      }
+    }
+    mma_commit(bar_s);
+  };
+  auto issue_pv = [&](int buf) {                  // O_tile = P1 V1 + P1 V2 + P2 V1 (P in S[buf])
+    tc_fence_after();
+    constexpr uint32_t idO = idesc_f16(128, 256, false, true);
+    const uint32_t pb = tmem + kSBuf * buf;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {               // 16 cells = 8 TMEM columns of fp16 pairs
+      const uint64_t v1 = smem_desc(sbase + kVfOff + kk * 2048, 8192, 1024);
+      const uint64_t v2 = smem_desc(sbase + kVfOff + 32768 + kk * 2048, 8192, 1024);
+      mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v1, idO, kk > 0 ? 1u : 0u);
+      mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v2, idO, 1u);
+      mma_f16_ta(tmem + kOCol, pb + kP2Col + 8 * kk, v1, idO, 1u);
+    }
+    mma_commit(bar_o);
+  };
+
+  // Pipeline, iteration i (S double-buffered in TMEM; Kf, Vf, O_tile single):
+  //   (a) wait QK(i), softmax(i)            -- the tensor core runs PV(i-1)
+  //   (b) wait PV(i-1), merge O_tile(i-1)
+  //   (c) convert K(i+1), issue QK(i+1)
+  //   (d) convert V(i), issue PV(i)         -- QK(i+1) runs meanwhile
+  //   then prefetch raw(i+2) into the stage V(i) came from.
   bool ok_tile[2] = {false, false};
   if (n_tiles > 0) ok_tile[0] = load_raw(0, 0);
   cp_async_commit();
@@ -372,167 +449,117 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   float o_run[64];                 // this part's 64 dims of the row's O (rotated space)
 #pragma unroll
   for (int i = 0; i < 64; ++i) o_run[i] = 0.0f;
-  float m_run = -INFINITY, l_part = 0.0f;
-  uint32_t phase = 0;
+  float m_run = -INFINITY, l_part = 0.0f, alpha = 1.0f, alpha_prev = 1.0f;
+  uint32_t phase_s = 0, phase_o = 0;
   bool failed = false;
+  uint32_t valid_bits = 0;         // bit (t & 1): tile t's page id was valid
+
+  auto wait_bar = [&](uint32_t bar, uint32_t& phase) -> bool {   // one warp polls, all synchronise
+    if (warp == 0 && !mbar_wait(bar, phase & 1)) failed = true;
+    ++phase;
+    if (__syncthreads_or(failed ? 1 : 0)) { failed = true; return false; }
+    tc_fence_after();
+    return true;
+  };
+  auto merge = [&]() {             // o_run = o_run * alpha_prev + O_tile (IEEE fp32)
+    float o[32];
+    tmem_ld32(tmem + lane_base + kOCol + 64 * part, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o_run[i] = fmaf(o_run[i], alpha_prev, o[i]);
+    tmem_ld32(tmem + lane_base + kOCol + 64 * part + 32, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o_run[32 + i] = fmaf(o_run[32 + i], alpha_prev, o[i]);
+    tc_fence_before();
+  };
+  auto stage_k = [&](int t) {      // (c): convert K(t) and issue QK(t)
+    cp_async_wait<0>();            // raw(t) is the most recently committed copy group
+    __syncthreads();
+    const bool ok = __syncthreads_and(ok_tile[t & 1] ? 1 : 0) != 0;
+    valid_bits = ok ? (valid_bits | (1u << (t & 1))) : (valid_bits & ~(1u << (t & 1)));
+    convert_k(t & 1);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) issue_qk(t & 1);
+  };
+
+  if (n_tiles > 0) stage_k(0);
 
   for (int it = 0; it < n_tiles; ++it) {
-    const int stage = it & 1;
-    cp_async_wait<1>();
-    __syncthreads();
-    const bool valid = __syncthreads_and(ok_tile[stage] ? 1 : 0) != 0;
-    if (!valid && tid == 0) record_status(p.status, K8V4_ERANGE);
-    const uint32_t raw = sbase + kRawOff + stage * kRawBytes;
-    // ---- dequantise into the operand tiles
-    if (valid) {
-      for (int i = tid; i < 64 * 16; i += kThreads) {            // K: (cell j, 16-byte chunk kk)
-        const int j = i >> 4, kk = i & 15;
-        const uint4 w = lds128(raw + j * 256 + 16 * kk);
-        uint32_t h[8];
-        i8x4_to_f16(w.x, h[0], h[1]);
-        i8x4_to_f16(w.y, h[2], h[3]);
-        i8x4_to_f16(w.z, h[4], h[5]);
-        i8x4_to_f16(w.w, h[6], h[7]);
-        const int dim = 16 * kk, chunk = dim >> 6, unit = (dim & 63) >> 3;
-        const uint32_t dst = sbase + kKfOff + chunk * 8192;
-        sts128(dst + swz(j, unit), h[0], h[1], h[2], h[3]);
-        sts128(dst + swz(j, unit + 1), h[4], h[5], h[6], h[7]);
-      }
-      {                                                          // V: (cell j, block b)
-        const int j = tid >> 3, b = tid & 7;
-        const uint4 w = lds128(raw + kRawK + j * 128 + 16 * b);
-        const __half dh = *reinterpret_cast<const __half*>(smem + kRawOff + stage * kRawBytes + kRawK + kRawV +
-                                                              kRawKs + 16 * j + 2 * b);
-        const __half2 d2 = __halves2half2(dh, dh);
-        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-        uint32_t lo[2][8], hi[2][8];   // [plane] dims 32b + (0..15) and 32b + 16 + (0..15), 8 pairs each
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t t01 = prmt(ws4[q], 0u, 0x5140u);   // {b0, 0, b1, 0}
-          const uint32_t t23 = prmt(ws4[q], 0u, 0x5342u);   // {b2, 0, b3, 0}
-          nib_vhat(t01, 0, d2, lo[0][2 * q], lo[1][2 * q]);
-          nib_vhat(t23, 0, d2, lo[0][2 * q + 1], lo[1][2 * q + 1]);
-          nib_vhat(t01, 4, d2, hi[0][2 * q], hi[1][2 * q]);
-          nib_vhat(t23, 4, d2, hi[0][2 * q + 1], hi[1][2 * q + 1]);
-        }
-        const int atom = b >> 1, unit0 = 4 * (b & 1);
-#pragma unroll
-        for (int pl = 0; pl < 2; ++pl) {
-          const uint32_t dst = sbase + kVfOff + pl * 32768 + atom * 8192;
-          sts128(dst + swz(j, unit0), lo[pl][0], lo[pl][1], lo[pl][2], lo[pl][3]);
-          sts128(dst + swz(j, unit0 + 1), lo[pl][4], lo[pl][5], lo[pl][6], lo[pl][7]);
-          sts128(dst + swz(j, unit0 + 2), hi[pl][0], hi[pl][1], hi[pl][2], hi[pl][3]);
-          sts128(dst + swz(j, unit0 + 3), hi[pl][4], hi[pl][5], hi[pl][6], hi[pl][7]);
-        }
-      }
-      if (tid < 64)      // K scales of the tile (the raw stage is refilled below)
-        reinterpret_cast<float2*>(smem + kKsBufOff)[tid] =
-            reinterpret_cast<const float2*>(smem + kRawOff + stage * kRawBytes + kRawK + kRawV)[tid];
-    }
-    fence_async_smem();
-    __syncthreads();
-    if (it + 2 < n_tiles) ok_tile[stage] = load_raw(it + 2, stage);
-    cp_async_commit();
-    if (!valid) continue;
-
-    // ---- S_h = Q_h K_h^T (fresh accumulators)
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t idS = idesc_f16(128, 64, false, false);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int chunk = 2 * h + (kk >> 2);
-          const uint32_t off = (kk & 3) * 32;
-          const uint64_t a = smem_desc(sbase + kQOff + chunk * 16384 + off, 16, 1024);
-          const uint64_t b = smem_desc(sbase + kKfOff + chunk * 8192 + off, 16, 1024);
-          mma_f16(tmem + (h ? kS1Col : kS0Col), a, b, idS, kk > 0 ? 1u : 0u);
-        }
-      }
-      mma_commit(bar_s);
-    }
-    if (!mbar_wait(bar_s, phase & 1)) failed = true;
-    tc_fence_after();
-    if (__syncthreads_or(failed ? 1 : 0)) { failed = true; break; }
-
-    // ---- scores of this part's 16 cells, row maximum across the four parts
+    const int buf = it & 1;
+    const bool valid_cur = (valid_bits >> buf) & 1u;
+    if (!valid_cur && tid == 0) record_status(p.status, K8V4_ERANGE);
+    // ---- (a) scores of tile it: this part's 16 cells, row max across the parts
+    if (!wait_bar(bar_s, phase_s)) break;
     const int cell0 = it * kTileN;
     float sc[16];
     {
       const float* ks = reinterpret_cast<const float*>(smem + kKsBufOff);
       float a[16], b[16];
-      tmem_ld16(tmem + lane_base + kS0Col + 16 * part, a);
-      tmem_ld16(tmem + lane_base + kS1Col + 16 * part, b);
-      const int vis = my_vis - cell0 - 16 * part;   // cells [0, vis) of this part are visible
+      tmem_ld16(tmem + lane_base + kSBuf * buf + kS0Col + 16 * part, a);
+      tmem_ld16(tmem + lane_base + kSBuf * buf + kS1Col + 16 * part, b);
+      const int vis = valid_cur ? my_vis - cell0 - 16 * part : 0;   // cells [0, vis) of this part
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int cc = 16 * part + c;
-        const float v = (ks[2 * cc] * a[c] + ks[2 * cc + 1] * b[c]) * my_f;
-        sc[c] = c < vis ? v : -INFINITY;
-        mx = fmaxf(mx, sc[c]);
+      for (int c = 0; c < 16; c += 2) {
+        const float4 k2 = *reinterpret_cast<const float4*>(ks + 2 * (16 * part + c));
+        const float v0 = (k2.x * a[c] + k2.y * b[c]) * my_f;
+        const float v1 = (k2.z * a[c + 1] + k2.w * b[c + 1]) * my_f;
+        sc[c] = c < vis ? v0 : -INFINITY;
+        sc[c + 1] = c + 1 < vis ? v1 : -INFINITY;
+        mx = fmaxf(mx, fmaxf(sc[c], sc[c + 1]));
       }
       red[part * kRows + row] = mx;
     }
     __syncthreads();
-    const float mt = fmaxf(fmaxf(red[row], red[kRows + row]), fmaxf(red[2 * kRows + row], red[3 * kRows + row]));
-    const float m_new = fmaxf(m_run, mt);
-    const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);   // 0 on the first visible tile
-    const float mu = m_new == -INFINITY ? 0.0f : m_new;
-    m_run = m_new;
     {
+      const float mt = fmaxf(fmaxf(red[row], red[kRows + row]), fmaxf(red[2 * kRows + row], red[3 * kRows + row]));
+      const float m_new = fmaxf(m_run, mt);
+      alpha_prev = alpha;
+      alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);   // 0 on the first visible tile
+      // p * 2^7 = exp2(s - m + 7); the 2^7 keeps small probabilities normal in fp16
+      const float mu = (m_new == -INFINITY ? 0.0f : m_new) - 7.0f;
+      m_run = m_new;
       float p1v[8], p2v[8];
       float psum = 0.0f;
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
-        const float a = __fmul_rn(exp2f(sc[c] - mu), kPScale), b = __fmul_rn(exp2f(sc[c + 1] - mu), kPScale);
-        const __half2 h1 = __floats2half2_rn(a, b);
-        const float2 f1 = __half22float2(h1);
-        const __half2 h2 = __floats2half2_rn(a - f1.x, b - f1.y);
-        const float2 f2 = __half22float2(h2);
-        psum += (f1.x + f2.x) + (f1.y + f2.y);  // l sums the probabilities the MMAs use
+        const float a = exp2f(sc[c] - mu), b = exp2f(sc[c + 1] - mu);
+        // hi plane: a rounded to 11 significant bits (exact in fp16 in the normal range)
+        const float ah = __uint_as_float((__float_as_uint(a) + 0x1000u) & 0xffffe000u);
+        const float bh = __uint_as_float((__float_as_uint(b) + 0x1000u) & 0xffffe000u);
+        const __half2 h1 = __floats2half2_rn(ah, bh);
+        const __half2 h2 = __floats2half2_rn(a - ah, b - bh);
+        psum += a + b;
         p1v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
         p2v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
       }
       l_part = l_part * alpha + psum;
-      // P planes overwrite S0's columns: every part has read its scores (barrier above)
-      tmem_st8(tmem + lane_base + kP1Col + 8 * part, p1v);
-      tmem_st8(tmem + lane_base + kP2Col + 8 * part, p2v);
+      // P planes overwrite S[buf]'s S0 columns: every part has read its scores (barrier above)
+      tmem_st8(tmem + lane_base + kSBuf * buf + kP1Col + 8 * part, p1v);
+      tmem_st8(tmem + lane_base + kSBuf * buf + kP2Col + 8 * part, p2v);
     }
     tc_fence_before();
+    // ---- (b) previous tile's O_tile into the register accumulator
+    if (it > 0) {
+      if (!wait_bar(bar_o, phase_o)) break;
+      merge();
+    }
+    // ---- (c) next tile's K and its scores
+    if (it + 1 < n_tiles) stage_k(it + 1);
+    // ---- (d) this tile's V and O_tile = P V
+    convert_v(buf);
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-
-    // ---- O_tile = P1 V1 + P1 V2 + P2 V1 (fresh accumulator every tile)
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t idO = idesc_f16(128, 256, false, true);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {             // 16 cells = 8 TMEM columns of fp16 pairs
-        const uint64_t v1 = smem_desc(sbase + kVfOff + kk * 2048, 8192, 1024);
-        const uint64_t v2 = smem_desc(sbase + kVfOff + 32768 + kk * 2048, 8192, 1024);
-        mma_f16_ta(tmem + kOCol, tmem + kP1Col + 8 * kk, v1, idO, kk > 0 ? 1u : 0u);
-        mma_f16_ta(tmem + kOCol, tmem + kP1Col + 8 * kk, v2, idO, 1u);
-        mma_f16_ta(tmem + kOCol, tmem + kP2Col + 8 * kk, v1, idO, 1u);
-      }
-      mma_commit(bar_o);
-    }
-    if (!mbar_wait(bar_o, phase & 1)) failed = true;
-    tc_fence_after();
-    phase ^= 1;
-    if (__syncthreads_or(failed ? 1 : 0)) { failed = true; break; }
-
-    // ---- merge: o_run = o_run * alpha + O_tile (IEEE fp32 on the CUDA cores)
-    {
-      float o[32];
-      tmem_ld32(tmem + lane_base + kOCol + 64 * part, o);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o_run[i] = fmaf(o_run[i], alpha, o[i]);
-      tmem_ld32(tmem + lane_base + kOCol + 64 * part + 32, o);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o_run[32 + i] = fmaf(o_run[32 + i], alpha, o[i]);
-    }
-    tc_fence_before();     // the next tile's MMAs overwrite these columns
+    if (tid == 0) issue_pv(buf);
+    if (it + 2 < n_tiles) ok_tile[buf] = load_raw(it + 2, buf);   // raw stage `buf` is consumed
+    cp_async_commit();
+  }
+  // ---- the last tile's O_tile
+  if (!failed && n_tiles > 0) {
+    alpha_prev = alpha;
+    if (wait_bar(bar_o, phase_o)) merge();
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -586,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   } else {
     if (tid == 0) {
       record_status(p.status, K8V4_ECUDA);
-      mma_commit(bar_o);                     // let in-flight MMAs drain (bounded)
-      (void)mbar_wait(bar_o, phase & 1);
+      mma_commit(bar_d);                     // let in-flight MMAs drain (bounded)
+      (void)mbar_wait(bar_d, 0);
     }
   }
   tc_fence_before();

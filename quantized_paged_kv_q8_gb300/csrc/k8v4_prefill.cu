@@ -99,6 +99,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
   return false;
 }
+// 2^x on the special-function unit (approximate, subnormal results flushed to 0)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -463,12 +469,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   };
   auto merge = [&]() {             // o_run = o_run * alpha_prev + O_tile (IEEE fp32)
     float o[32];
-    tmem_ld32(tmem + lane_base + kOCol + 64 * part, o);
+    const float2 a2 = make_float2(alpha_prev, alpha_prev);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o_run[i] = fmaf(o_run[i], alpha_prev, o[i]);
-    tmem_ld32(tmem + lane_base + kOCol + 64 * part + 32, o);
+    for (int h = 0; h < 2; ++h) {
+      tmem_ld32(tmem + lane_base + kOCol + 64 * part + 32 * h, o);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o_run[32 + i] = fmaf(o_run[32 + i], alpha_prev, o[i]);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 r = __ffma2_rn(make_float2(o_run[32 * h + i], o_run[32 * h + i + 1]), a2, make_float2(o[i], o[i + 1]));
+        o_run[32 * h + i] = r.x;
+        o_run[32 * h + i + 1] = r.y;
+      }
+    }
     tc_fence_before();
   };
   auto stage_k = [&](int t) {      // (c): convert K(t) and issue QK(t)
@@ -499,17 +510,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       tmem_ld16(tmem + lane_base + kSBuf * buf + kS0Col + 16 * part, a);
       tmem_ld16(tmem + lane_base + kSBuf * buf + kS1Col + 16 * part, b);
       const int vis = valid_cur ? my_vis - cell0 - 16 * part : 0;   // cells [0, vis) of this part
+      // sc holds the unscaled scores; my_f > 0, so the maximum commutes with it
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
         const float4 k2 = *reinterpret_cast<const float4*>(ks + 2 * (16 * part + c));
-        const float v0 = (k2.x * a[c] + k2.y * b[c]) * my_f;
-        const float v1 = (k2.z * a[c + 1] + k2.w * b[c + 1]) * my_f;
-        sc[c] = c < vis ? v0 : -INFINITY;
-        sc[c + 1] = c + 1 < vis ? v1 : -INFINITY;
-        mx = fmaxf(mx, fmaxf(sc[c], sc[c + 1]));
+        sc[c] = k2.x * a[c] + k2.y * b[c];
+        sc[c + 1] = k2.z * a[c + 1] + k2.w * b[c + 1];
       }
-      red[part * kRows + row] = mx;
+      if (vis < 16) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) sc[c] = c < vis ? sc[c] : -INFINITY;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) mx = fmaxf(mx, sc[c]);
+      red[part * kRows + row] = mx * my_f;
     }
     __syncthreads();
     {
@@ -521,20 +536,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       const float mu = (m_new == -INFINITY ? 0.0f : m_new) - 7.0f;
       m_run = m_new;
       float p1v[8], p2v[8];
-      float psum = 0.0f;
+      float2 psum2 = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
-        const float a = exp2f(sc[c] - mu), b = exp2f(sc[c + 1] - mu);
+        const float a = ex2_ftz(fmaf(sc[c], my_f, -mu)), b = ex2_ftz(fmaf(sc[c + 1], my_f, -mu));
         // hi plane: a rounded to 11 significant bits (exact in fp16 in the normal range)
         const float ah = __uint_as_float((__float_as_uint(a) + 0x1000u) & 0xffffe000u);
         const float bh = __uint_as_float((__float_as_uint(b) + 0x1000u) & 0xffffe000u);
         const __half2 h1 = __floats2half2_rn(ah, bh);
         const __half2 h2 = __floats2half2_rn(a - ah, b - bh);
-        psum += a + b;
+        psum2 = __fadd2_rn(psum2, make_float2(a, b));
         p1v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
         p2v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
       }
-      l_part = l_part * alpha + psum;
+      l_part = l_part * alpha + (psum2.x + psum2.y);
       // P planes overwrite S[buf]'s S0 columns: every part has read its scores (barrier above)
       tmem_st8(tmem + lane_base + kSBuf * buf + kP1Col + 8 * part, p1v);
       tmem_st8(tmem + lane_base + kSBuf * buf + kP2Col + 8 * part, p2v);

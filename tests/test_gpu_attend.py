@@ -62,6 +62,39 @@ def test_decode_32k():
     assert np.array_equal(gpu.pages.cpu().numpy(), ref.buf)
 
 
+def test_decode_wide_v_scales():
+    """V rows whose q4_0 scales reach |d| >= 256 (values in the thousands) mixed
+    with ordinary rows: tiles holding one are read through the wide-scale path of
+    the decode PV, the others through the narrow one.  An output element here is
+    a sum of terms up to ~1e4 that cancel down to ~1, which no fp32 sum resolves
+    to 2e-5 of the small result, so the bar is norm-wise: 2e-5 of the largest
+    |ref| of the row (the fp32 rounding scale of its terms)."""
+    w = synth.decode_workload(synth.config_seed(2) + 9, 3000, P=64)
+    v = w.v.f32.copy()
+    v[100:400] *= 5000.0           # whole tiles of wide scales
+    v[1000::37] *= 3000.0          # one wide cell in many otherwise narrow tiles
+    v[2000:2100] *= 1e-6           # tiny scales (subnormal fp16 d) next to them
+    gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv)
+    pt_d = append_both(gpu, ref, w.page_table, w.pos, synth.Tensor(w.k.f32[None], w.dtype),
+                       synth.Tensor(v[None], w.dtype))
+    got = decode_gpu(gpu, dev_tensor(w.q, (1, 16, 256)), pt_d, w.seq_lens, 3000)
+    rs, rh, rv = oracle.decode_rows(1, 16, w.seq_lens)
+    want = ref.attention(w.page_table, rs, rh, rv, w.q.f32.reshape(-1, 256))
+    assert np.abs(want).max() > 100.0          # the wide rows carry weight
+    assert _normwise(got.reshape(-1, 256), want) <= TOL
+    # and a length that ends inside the wide run
+    got = decode_gpu(gpu, dev_tensor(w.q, (1, 16, 256)), pt_d, np.array([250], np.int32), 3000)
+    rs, rh, rv = oracle.decode_rows(1, 16, [250])
+    want = ref.attention(w.page_table, rs, rh, rv, w.q.f32.reshape(-1, 256))
+    assert _normwise(got.reshape(-1, 256), want) <= TOL
+
+
+def _normwise(got: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of max |got - ref| / max(1, max |ref|)."""
+    e = np.abs(got.astype(np.float64) - ref).max(axis=1)
+    return float((e / np.maximum(1.0, np.abs(ref).max(axis=1))).max())
+
+
 def test_decode_zero_length_rows_are_zero():
     w = synth.decode_workload(synth.config_seed(2) + 8, 200, P=16)
     gpu, ref, _ = _single_seq(w)

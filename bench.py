@@ -52,6 +52,23 @@ def dist_info():
     return ws, rank, local
 
 
+def job_timing(total_ms: float, steps: int, cells_per_rank: int, device=None):
+    """Whole-job timing of a replicated step: the slowest rank's wall time over
+    `steps` steps sets the step time (an all-reduce MAX when a process group is
+    up), and the rate counts the cells of every rank.  Returns (ms per step,
+    cells/s of the job, world size)."""
+    import torch
+    world = 1
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        world = torch.distributed.get_world_size()
+        if world > 1:
+            t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            total_ms = float(t.item())
+    ms_step = total_ms / steps
+    return ms_step, world * cells_per_rank / (ms_step / 1e3), world
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -380,12 +397,7 @@ def main():
     total_ms = t0.elapsed_time(t1)
     dec_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     assert k8.k8v4_last_device_status() == 0
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    ms_step = total_ms / K
-    cells_per_s = world * N_CELLS / (ms_step / 1e3)
+    ms_step, cells_per_s, _ = job_timing(total_ms, K, N_CELLS, dev)
     value = cells_per_s * CELL_BYTES / 1e9
 
     if args.profile:

@@ -678,9 +678,15 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
   const dim3 grid(plan.splits, p.C.H, p.n_seqs);
   kern<<<grid, plan.warps * 32, smem, L.stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
-  // combine: a programmatic dependent launch, so its launch overlaps the tail
-  // of the split kernel; it waits (griddepcontrol.wait) for the partials
-  const int rows = p.n_seqs * p.n_q * p.C.H * kGqa;
+  return launch_combine(L, p.ws, plan.splits, p.n_seqs, p.n_q, p.C.H, out);
+}
+
+}  // namespace
+
+// The combine is a programmatic dependent launch, so its launch overlaps the
+// tail of the split kernel; it waits (griddepcontrol.wait) for the partials.
+int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out) {
+  const int rows = n_seqs * n_q * H * kGqa;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows, kD / 32);
   cfg.blockDim = dim3(256);
@@ -691,15 +697,13 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(p.ws), plan.splits, p.n_q,
-                         p.C.H * kGqa, out) != cudaSuccess)
-    return K8V4_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, combine_kernel, ws, splits, n_q, H * kGqa, out) != cudaSuccess) return K8V4_ECUDA;
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
 }
 
-}  // namespace
-
 AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
+  // several queries per sequence over a k8v4 cache: tiles dequantised once, shared by the query warps
+  if (n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) return plan_verify(C, n_seqs, n_q, max_seq_len, num_sms);
   AttendPlan pl{};
   pl.n_q = n_q;
   pl.n_groups = n_q >= kWarps ? 1 : kWarps / n_q;
@@ -725,6 +729,8 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
                   float sm_scale, float* out, void* ws) {
   if (n_seqs == 0) return K8V4_OK;
+  if (plan.n_q > 1 && C.fmt == K8V4_FORMAT_K8V4)
+    return launch_verify(L, C, plan, q, q_dtype, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
   AttendParams p;
   p.C = C;
   p.q = q;

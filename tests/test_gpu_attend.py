@@ -128,6 +128,37 @@ def test_verify_small(n_q):
     assert rel_err(got.reshape(-1, 256), want) <= TOL
 
 
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8])
+def test_verify_irregular_steps_p16_fp32(fmt):
+    """Verify over 16-cell pages with fp32 queries and irregular per-query steps
+    (0, 1, a page edge, mid-tile, the whole sequence): three sequences, 7
+    queries each, every row checked."""
+    seed = synth.config_seed(4) + 77
+    P, H, n_q = 16, 2, 7
+    lens = np.array([1500, 33, 700], np.int32)
+    pt, n_pages = synth.interleaved_pool(seed, lens, P)
+    ks = [synth.kv_values(seed, synth.T_K, b, int(n), H, 3, "bf16") for b, n in enumerate(lens)]
+    vs = [synth.kv_values(seed, synth.T_V, b, int(n), H, 3, "bf16") for b, n in enumerate(lens)]
+    qs = [synth.q_values(seed, b, n_q, H, "f32") for b in range(len(lens))]
+    steps = np.array([[0, 1, 16, 17, 499, 1499, 1500],
+                      [33, 0, 1, 31, 32, 16, 15],
+                      [700, 699, 64, 65, 0, 2, 350]], np.int32)
+    gpu, ref = make_caches(n_pages, P, H, fmt)
+    pt_d = torch.from_numpy(pt).cuda()
+    for b in range(len(lens)):
+        append_both(gpu, ref, pt[b:b + 1], np.array([0]), synth.Tensor(ks[b].f32[None], "bf16"),
+                    synth.Tensor(vs[b].f32[None], "bf16"))
+    q = torch.stack([dev_tensor(qs[b]) for b in range(len(lens))])
+    got = verify_gpu(gpu, q, pt_d, steps, int(lens.max()))
+    assert k8.k8v4_last_device_status() == 0
+    rs, rh, rv = oracle.multi_query_rows(steps, 16)
+    qrows = np.concatenate([qs[b].f32.reshape(-1, 256) for b in range(len(lens))])
+    want = ref.attention(pt, rs, rh, rv, qrows)
+    got = got.reshape(-1, 256)
+    assert np.all(got[rv == 0] == 0.0)
+    assert rel_err(got, want) <= TOL
+
+
 def test_verify_rows_equal_decode_at_step():
     """Mode cross-check on the GPU: verify query i equals decode with seq_len =
     len - 4 + i (same q, same cache) within the tolerance."""

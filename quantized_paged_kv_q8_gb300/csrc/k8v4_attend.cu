@@ -602,70 +602,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- combine
-// Weighted sum of the splits' (already un-rotated) partials.  One CTA per
-// (output row, 32-dim chunk): the split maxima and weights are reduced first,
-// then warp w sums splits w, w+8, ... for its lane's dim with independent loads,
-// and the eight warp sums are added in shared memory.  Launched as a
-// programmatic dependent of the split kernel (griddepcontrol.wait).
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws, int splits, int n_q, int HQ,
-                                                      float* __restrict__ out) {
-  constexpr int kMaxSplitsInSmem = 1024;
-  __shared__ float wgt[kMaxSplitsInSmem];
-  __shared__ float red[8][33];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int row = blockIdx.x, chunk = blockIdx.y;   // row = (b, qi, head)
-  const int head = row % HQ;
-  const int bq = row / HQ;
-  const int b = bq / n_q, qi = bq % n_q;
-  const int64_t stride = static_cast<int64_t>(n_q) * HQ * kPStride;     // between splits
-  const float* base = ws + ((static_cast<int64_t>(b) * splits * n_q + qi) * HQ + head) * kPStride;
-  // pass 1: M = max_s m_s
-  float M = -INFINITY;
-  for (int s = t; s < splits; s += 256) M = fmaxf(M, base[s * stride + 256]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  if (lane == 0) red[warp][32] = M;
-  __syncthreads();
-  M = red[0][32];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w][32]);
-  __syncthreads();
-  // weights w_s = exp2(m_s - M) and L = sum_s l_s w_s
-  float L = 0.0f;
-  for (int s = t; s < splits; s += 256) {
-    const float ms = base[s * stride + 256];
-    const float w = (M == -INFINITY || ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-    if (s < kMaxSplitsInSmem) wgt[s] = w;
-    L += base[s * stride + 257] * w;
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
-  if (lane == 0) red[warp][32] = L;
-  __syncthreads();
-  L = 0.0f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) L += red[w][32];
-  // pass 2: sum of weighted partials for dim chunk*32 + lane
-  const int dim = chunk * 32 + lane;
-  float acc = 0.0f;
-#pragma unroll 4
-  for (int s = warp; s < splits; s += 8) {
-    const float w = s < kMaxSplitsInSmem ? wgt[s] : ((M == -INFINITY || base[s * stride + 256] == -INFINITY)
-                                                          ? 0.0f : exp2f(base[s * stride + 256] - M));
-    acc += base[s * stride + dim] * w;
-  }
-  red[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    float v = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += red[w][lane];
-    out[static_cast<int64_t>(row) * kD + dim] = L > 0.0f ? v / L : 0.0f;
-  }
-}
-
 template <int FMT, bool QF32, bool NQ1>
 int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, float* out) {
   const size_t stage_bytes = static_cast<size_t>(plan.n_groups) * kStages * Stage<FMT>::kBytes +
@@ -682,24 +618,6 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
 }
 
 }  // namespace
-
-// The combine is a programmatic dependent launch, so its launch overlaps the
-// tail of the split kernel; it waits (griddepcontrol.wait) for the partials.
-int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out) {
-  const int rows = n_seqs * n_q * H * kGqa;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows, kD / 32);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = L.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel, ws, splits, n_q, H * kGqa, out) != cudaSuccess) return K8V4_ECUDA;
-  return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
-}
 
 AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
   // several queries per sequence over a k8v4 cache: tiles dequantised once, shared by the query warps

@@ -130,6 +130,13 @@ __device__ __forceinline__ uint32_t i8_to_bf16(uint32_t r, uint32_t s0, uint32_t
   return prmt(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
 }
 
+// 2^x on the special-function unit (relative error ~2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- tile loader
 // Stage one 16-cell tile of KV head g (cells slot0 .. slot0+15 of one page) with
 // 16-byte cp.async copies.  NTHR > 0 fixes the group size at compile time (the
@@ -392,12 +399,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
       t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, off));
     }
     const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);   // finite: cell0 is visible
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
     float pr[4];
-    pr[0] = exp2f(sc[0] - mn0);
-    pr[1] = exp2f(sc[1] - mn1);
-    pr[2] = exp2f(sc[2] - mn0);
-    pr[3] = exp2f(sc[3] - mn1);
+    pr[0] = ex2(sc[0] - mn0);
+    pr[1] = ex2(sc[1] - mn1);
+    pr[2] = ex2(sc[2] - mn0);
+    pr[3] = ex2(sc[3] - mn1);
     l0 = l0 * al0 + (pr[0] + pr[2]);
     l1 = l1 * al1 + (pr[1] + pr[3]);
     m0 = mn0;
@@ -405,7 +412,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
-        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+        const float2 al = make_float2(al0, al1);
+        const float2 x = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), al);
+        const float2 y = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), al);
+        o[mt][0] = x.x; o[mt][1] = x.y; o[mt][2] = y.x; o[mt][3] = y.y;
       }
     }
 

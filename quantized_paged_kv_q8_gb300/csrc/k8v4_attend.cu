@@ -189,6 +189,9 @@ __device__ __forceinline__ void load_tile(const CacheView& C, uint32_t s, const 
 template <int FMT, bool QF32, bool NQ1>
 __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const AttendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // launched as a programmatic dependent of the previous kernel in the stream
+  // (typically the append of the new token): nothing is read before it completes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   using S = Stage<FMT>;
   constexpr int kMT = 16;                                 // PV m-tiles (16 dims each)
   constexpr int kBlocks = FMT == K8V4_FORMAT_K8V4 ? 8 : 2; // scale blocks per head
@@ -621,8 +624,19 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
   auto kern = attend_splitk_kernel<FMT, QF32, NQ1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return K8V4_ECUDA;
-  const dim3 grid(plan.splits, p.C.H, p.n_seqs);
-  kern<<<grid, plan.warps * 32, smem, L.stream>>>(p);
+  // programmatic dependent launch: the CTAs are placed while the previous kernel
+  // (the new token's append) finishes; the kernel's first act is griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.splits, p.C.H, p.n_seqs);
+  cfg.blockDim = dim3(plan.warps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return K8V4_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
   return launch_combine(L, p.ws, plan.splits, p.n_seqs, p.n_q, p.C.H, out);
 }

@@ -644,8 +644,16 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
 }  // namespace
 
 AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
-  // several queries per sequence over a k8v4 cache: tiles dequantised once, shared by the query warps
-  if (n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) return plan_verify(C, n_seqs, n_q, max_seq_len, num_sms);
+  // several queries per sequence over a k8v4 cache: tiles dequantised once and
+  // shared by all queries -- on the tcgen05 kernel (bf16 q, pages of 64k cells)
+  // or on the warp-MMA verify kernel; the workspace covers either
+  if (n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) {
+    const AttendPlan mw = plan_verify(C, n_seqs, n_q, max_seq_len, num_sms);
+    if (C.P % 64 != 0) return mw;
+    AttendPlan tc = plan_verify_tc(C, n_seqs, n_q, max_seq_len, num_sms);
+    tc.ws_bytes = std::max(tc.ws_bytes, mw.ws_bytes);
+    return tc;
+  }
   AttendPlan pl{};
   pl.n_q = n_q;
   pl.n_groups = n_q >= kWarps ? 1 : kWarps / n_q;
@@ -671,8 +679,12 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
                   float sm_scale, float* out, void* ws) {
   if (n_seqs == 0) return K8V4_OK;
-  if (plan.n_q > 1 && C.fmt == K8V4_FORMAT_K8V4)
-    return launch_verify(L, C, plan, q, q_dtype, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
+  if (plan.n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) {
+    if (q_dtype == K8V4_BF16 && C.P % 64 == 0)
+      return launch_verify_tc(L, C, plan, q, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
+    const AttendPlan mw = plan_verify(C, n_seqs, plan.n_q, max_seq_len, L.num_sms);
+    return launch_verify(L, C, mw, q, q_dtype, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
+  }
   AttendParams p;
   p.C = C;
   p.q = q;

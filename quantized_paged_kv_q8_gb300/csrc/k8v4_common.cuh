@@ -96,6 +96,10 @@ AttendPlan plan_verify(const CacheView& C, int n_seqs, int n_q, int max_seq_len,
 int launch_verify(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
                   float sm_scale, float* out, void* ws);
+AttendPlan plan_verify_tc(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms);
+int launch_verify_tc(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q,
+                     const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
+                     float sm_scale, float* out, void* ws);
 // weighted sum of split partials (o[256], m, l rows of 260 floats) -> out, launched programmatically dependent
 int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out);
 int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,

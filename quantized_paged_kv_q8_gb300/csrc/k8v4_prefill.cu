@@ -19,12 +19,17 @@
 //      S, apply the K scales and the online softmax (log2 domain), and write
 //      P * 2^7 back into TMEM (over S) as two fp16 planes P1 = RN(P),
 //      P2 = RN(P - P1) (22 significant bits);
-//   5. one thread issues O_tile = P1 V1 + P1 V2 + P2 V1 into a fresh TMEM
-//      accumulator (A from TMEM, M=128, N=256, K=16; the dropped P2 V2 term is
-//      below 2^-22 of the product), and every thread folds its 64 dims of
-//      O_tile into an fp32 register accumulator: o = o * alpha + O_tile.
-//      Accumulating all tiles inside TMEM instead would let the tensor core's
-//      per-instruction accumulation rounding build up over thousands of steps.
+//   5. one thread issues O_tile += P1 V1 + P1 V2 + P2 V1 (A from TMEM, M=128,
+//      N=256, K=16; the dropped P2 V2 term is below 2^-22 of the product).
+//      P is taken against a per-row reference maximum that moves only when a
+//      tile's maximum exceeds it by more than 2^8 (so P * 2^7 <= 2^15 stays in
+//      fp16); while no row moves its reference, consecutive tiles accumulate in
+//      the same TMEM tile.  When some row moves it, or after kChain tiles, every
+//      thread folds its 64 dims of O_tile into an fp32 register accumulator,
+//      o = (o + O_tile) * 2^(m_old - m_new), and the next tile starts a fresh
+//      TMEM tile: accumulating all tiles inside TMEM would let the tensor
+//      core's per-instruction accumulation rounding build up over thousands of
+//      steps.
 // fp16 operands with one rounding would leave errors near 1e-4 at 2^18 cells,
 // above the 2e-5 bar; the split planes bring them to the fp32 level.
 // The epilogue divides by l, applies the inverse Walsh-Hadamard transform
@@ -33,6 +38,8 @@
 // Every mbarrier wait is bounded: on timeout the kernel records an error in the
 // device status word, stops issuing work, waits (bounded) for its own
 // outstanding copies and MMAs, frees its TMEM and returns.
+#include <algorithm>
+
 #include "k8v4_common.cuh"
 
 namespace k8v4 {
@@ -67,16 +74,20 @@ constexpr uint32_t kTmemCols = 512;    // S buffers [0,128) and [128,256) (S0 | 
                                        // the buffer's S0 columns), O_tile [256,512)
 constexpr uint32_t kSBuf = 128, kS0Col = 0, kS1Col = 64, kOCol = 256, kP1Col = 0, kP2Col = 32;
 constexpr uint32_t kSpinLimit = 1u << 22;     // ~1 s of try_wait polling
+constexpr float kSlack = 8.0f;                // log2 headroom of P above its row's reference maximum
+constexpr int kChain = 4;                     // tiles accumulated in one TMEM O tile at most
 
 struct PrefillParams {
   CacheView C;
-  const uint16_t* q;       // bf16 [n_q_tok][HQ][256]
-  const int32_t* pt;       // [max_pages]
+  const uint16_t* q;       // bf16 [n_seqs][n_q_tok][HQ][256]
+  const int32_t* pt;       // [n_seqs][max_pages]
   int64_t max_pages;
-  const int32_t* steps;    // [n_q_tok] or null
+  const int32_t* steps;    // [n_seqs][n_q_tok] or null (causal)
   int seq_len, n_q_tok;
+  int splits, cells_per_split;   // split-K over the cells (1 split: the whole range)
   float sm_scale_log2;
-  float* out;
+  float* out;              // final rows [n_seqs][n_q_tok][HQ][256], or null
+  float* ws;               // else partial rows (o[256], m, l) for the combine
   int* status;
 };
 
@@ -237,8 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   const int row = tid & (kRows - 1), part = tid >> 7;
   const int g = blockIdx.y;
   const int tok0 = blockIdx.x * kTokens;
+  const int b = blockIdx.z / p.splits, split = blockIdx.z % p.splits;
   const CacheView& C = p.C;
   const int HQ = C.H * kGqa;
+  const int32_t* pt = p.pt + static_cast<int64_t>(b) * p.max_pages;
+  const uint16_t* qs = p.q + static_cast<int64_t>(b) * p.n_q_tok * HQ * kD;
 
   const uint32_t bar_s = sbase + kBarOff, bar_o = sbase + kBarOff + 8, bar_d = sbase + kBarOff + 32;
   const uint32_t tmem_slot = sbase + kBarOff + 16;
@@ -251,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   {
     const int t = tok0 + row / kGqa;
     if (t < p.n_q_tok) {
-      int v = p.steps ? p.steps[t] : p.seq_len - p.n_q_tok + t + 1;
+      int v = p.steps ? p.steps[static_cast<int64_t>(b) * p.n_q_tok + t] : p.seq_len - p.n_q_tok + t + 1;
       if (v < 0 || v > p.seq_len) {
         if (part == 0) record_status(p.status, K8V4_ERANGE);
         v = v < 0 ? 0 : p.seq_len;
@@ -264,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     mbar_init(bar_o, 1);
     mbar_init(bar_d, 1);
     *nmax_s = 0;
+    *reinterpret_cast<int*>(smem + kBarOff + 24) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     const int t = tok0 + row / kGqa, h = row % kGqa;
     uint4 raw[8];
     if (t < p.n_q_tok) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(t) * HQ + g * kGqa + h) * kD + 64 * part);
+      const uint4* src = reinterpret_cast<const uint4*>(qs + (static_cast<int64_t>(t) * HQ + g * kGqa + h) * kD + 64 * part);
 #pragma unroll
       for (int i = 0; i < 8; ++i) raw[i] = src[i];
     } else {
@@ -317,8 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   }
   __syncthreads();
   const float my_f = fsc[row];
-  const int n_max = *nmax_s;
-  const int n_tiles = (n_max + kTileN - 1) / kTileN;
+  // this CTA's tiles: [tile_lo, tile_lo + n_tiles) of the cells visible to any row
+  const int c_begin = split * p.cells_per_split;
+  const int c_end = min(*nmax_s, c_begin + p.cells_per_split);
+  const int tile_lo = c_begin / kTileN;
+  const int n_tiles = c_end > c_begin ? (c_end - c_begin + kTileN - 1) / kTileN : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -328,12 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   // ---- raw tile loader (all threads, 16-byte cp.async)
   // page ids are read one load ahead (tiles are staged in order 0, 1, 2, ...)
   auto fetch_page = [&](int tile) -> int64_t {
-    const int64_t pidx = static_cast<int64_t>(tile) * kTileN / C.P;
-    return (tile < n_tiles && pidx < p.max_pages) ? static_cast<int64_t>(p.pt[pidx]) : -1;
+    const int64_t pidx = static_cast<int64_t>(tile_lo + tile) * kTileN / C.P;
+    return (tile < n_tiles && pidx < p.max_pages) ? static_cast<int64_t>(pt[pidx]) : -1;
   };
   int64_t pf_page = fetch_page(0);
   auto load_raw = [&](int tile, int stage) {
-    const int cell0 = tile * kTileN;
+    const int cell0 = (tile_lo + tile) * kTileN;
     const uint32_t dst = sbase + kRawOff + stage * kRawBytes;
     const int64_t page = pf_page;
     pf_page = fetch_page(tile + 1);
@@ -425,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     }
     mma_commit(bar_s);
   };
-  auto issue_pv = [&](int buf) {                  // O_tile = P1 V1 + P1 V2 + P2 V1 (P in S[buf])
+  auto issue_pv = [&](int buf, bool fresh) {      // O_tile (+)= P1 V1 + P1 V2 + P2 V1 (P in S[buf])
     tc_fence_after();
     constexpr uint32_t idO = idesc_f16(128, 256, false, true);
     const uint32_t pb = tmem + kSBuf * buf;
@@ -433,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     for (int kk = 0; kk < 4; ++kk) {               // 16 cells = 8 TMEM columns of fp16 pairs
       const uint64_t v1 = smem_desc(sbase + kVfOff + kk * 2048, 8192, 1024);
       const uint64_t v2 = smem_desc(sbase + kVfOff + 32768 + kk * 2048, 8192, 1024);
-      mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v1, idO, kk > 0 ? 1u : 0u);
+      mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v1, idO, (kk > 0 || !fresh) ? 1u : 0u);
       mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v2, idO, 1u);
       mma_f16_ta(tmem + kOCol, pb + kP2Col + 8 * kk, v1, idO, 1u);
     }
@@ -455,11 +473,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   float o_run[64];                 // this part's 64 dims of the row's O (rotated space)
 #pragma unroll
   for (int i = 0; i < 64; ++i) o_run[i] = 0.0f;
-  float m_run = -INFINITY, l_part = 0.0f, alpha = 1.0f, alpha_prev = 1.0f;
+  float m_run = -INFINITY, l_part = 0.0f, alpha = 1.0f;   // m_run: the row's reference maximum
+  bool need = false;               // this row moved its reference on the current tile
+  int chain = 0;                   // tiles in the current TMEM O tile
+  int* flag_s = reinterpret_cast<int*>(smem + kBarOff + 24);   // a wait timed out (set by warp 0)
   uint32_t phase_s = 0, phase_o = 0;
   bool failed = false;
   uint32_t valid_bits = 0;         // bit (t & 1): tile t's page id was valid
 
+  // wait on `bar` (warp 0 polls) and OR `pred` over the CTA: 1 / 0, or -1 on timeout
+  auto wait_bar_or = [&](uint32_t bar, uint32_t& phase, bool pred) -> int {
+    if (warp == 0 && !mbar_wait(bar, phase & 1) && lane == 0) *reinterpret_cast<volatile int*>(flag_s) = 1;
+    ++phase;
+    const int any = __syncthreads_or(pred ? 1 : 0);
+    if (*reinterpret_cast<volatile int*>(flag_s)) { failed = true; return -1; }
+    tc_fence_after();
+    return any;
+  };
   auto wait_bar = [&](uint32_t bar, uint32_t& phase) -> bool {   // one warp polls, all synchronise
     if (warp == 0 && !mbar_wait(bar, phase & 1)) failed = true;
     ++phase;
@@ -467,15 +497,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     tc_fence_after();
     return true;
   };
-  auto merge = [&]() {             // o_run = o_run * alpha_prev + O_tile (IEEE fp32)
+  auto merge = [&](float a) {      // o_run = (o_run + O_tile) * a (IEEE fp32)
     float o[32];
-    const float2 a2 = make_float2(alpha_prev, alpha_prev);
+    const float2 a2 = make_float2(a, a);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       tmem_ld32(tmem + lane_base + kOCol + 64 * part + 32 * h, o);
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
-        const float2 r = __ffma2_rn(make_float2(o_run[32 * h + i], o_run[32 * h + i + 1]), a2, make_float2(o[i], o[i + 1]));
+        const float2 r = __fmul2_rn(__fadd2_rn(make_float2(o_run[32 * h + i], o_run[32 * h + i + 1]),
+                                               make_float2(o[i], o[i + 1])), a2);
         o_run[32 * h + i] = r.x;
         o_run[32 * h + i + 1] = r.y;
       }
@@ -502,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     if (!valid_cur && tid == 0) record_status(p.status, K8V4_ERANGE);
     // ---- (a) scores of tile it: this part's 16 cells, row max across the parts
     if (!wait_bar(bar_s, phase_s)) break;
-    const int cell0 = it * kTileN;
+    const int cell0 = (tile_lo + it) * kTileN;
     float sc[16];
     {
       const float* ks = reinterpret_cast<const float*>(smem + kKsBufOff);
@@ -529,10 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     __syncthreads();
     {
       const float mt = fmaxf(fmaxf(red[row], red[kRows + row]), fmaxf(red[2 * kRows + row], red[3 * kRows + row]));
-      const float m_new = fmaxf(m_run, mt);
-      alpha_prev = alpha;
-      alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);   // 0 on the first visible tile
-      // p * 2^7 = exp2(s - m + 7); the 2^7 keeps small probabilities normal in fp16
+      // the reference moves only when the tile's maximum exceeds it by more than
+      // kSlack (always on the row's first visible tile: m_run = -inf)
+      need = mt > m_run + kSlack;
+      const float m_new = need ? mt : m_run;
+      alpha = need ? exp2f(m_run - m_new) : 1.0f;                  // 0 on the first visible tile
+      // p * 2^7 = exp2(s - m + 7) <= 2^15; the 2^7 keeps small probabilities normal in fp16
       const float mu = (m_new == -INFINITY ? 0.0f : m_new) - 7.0f;
       m_run = m_new;
       float p1v[8], p2v[8];
@@ -555,11 +588,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       tmem_st8(tmem + lane_base + kSBuf * buf + kP2Col + 8 * part, p2v);
     }
     tc_fence_before();
-    // ---- (b) previous tile's O_tile into the register accumulator
+    // ---- (b) PV(it-1) done (Vf is free again); if some row moved its reference
+    // (or the chain is long), fold the TMEM O tile into the registers
+    bool fresh = true;
     if (it > 0) {
-      if (!wait_bar(bar_o, phase_o)) break;
-      merge();
+      const int any = wait_bar_or(bar_o, phase_o, need || chain >= kChain);
+      if (any < 0) break;
+      fresh = any != 0;
+      if (fresh) merge(alpha);
     }
+    chain = fresh ? 1 : chain + 1;
     // ---- (c) next tile's K and its scores
     if (it + 1 < n_tiles) stage_k(it + 1);
     // ---- (d) this tile's V and O_tile = P V
@@ -567,14 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) issue_pv(buf);
+    if (tid == 0) issue_pv(buf, fresh);
     if (it + 2 < n_tiles) ok_tile[buf] = load_raw(it + 2, buf);   // raw stage `buf` is consumed
     cp_async_commit();
   }
   // ---- the last tile's O_tile
   if (!failed && n_tiles > 0) {
-    alpha_prev = alpha;
-    if (wait_bar(bar_o, phase_o)) merge();
+    if (wait_bar(bar_o, phase_o)) merge(1.0f);
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -584,7 +621,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     red[part * kRows + row] = l_part;
     __syncthreads();
     const float l = (red[row] + red[kRows + row]) + (red[2 * kRows + row] + red[3 * kRows + row]);
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;    // O and l both carry the 2^7 factor of P
+    // final rows: O / l (both carry the 2^7 factor of P); partial rows keep O, m and l
+    const float inv = p.ws ? 1.0f : (l > 0.0f ? 1.0f / l : 0.0f);
+    if (p.ws && part == 0) fsc[row] = l;             // the row's l for the partial writer
+    float* mrow = reinterpret_cast<float*>(smem + kRedOff);        // red is free again after the read above
+    __syncthreads();
+    if (p.ws && part == 0) mrow[row] = m_run;
     float* rowbuf = reinterpret_cast<float*>(smem + kKfOff);     // [128][256] fp32, rotated by 4 * row
 #pragma unroll
     for (int i = 0; i < 64; i += 4) {
@@ -621,9 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
           v[e] = upper ? x - v[e] : v[e] + x;
         }
       }
-      float* dst = p.out + (static_cast<int64_t>(t) * HQ + g * kGqa + h) * kD + 8 * lane;
-      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0] * 0.0625f, v[1] * 0.0625f, v[2] * 0.0625f, v[3] * 0.0625f);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4] * 0.0625f, v[5] * 0.0625f, v[6] * 0.0625f, v[7] * 0.0625f);
+      float* dst = p.ws ? p.ws + ((((static_cast<int64_t>(b) * p.splits + split) * p.n_q_tok + t) * HQ) + g * kGqa + h) * 260
+                        : p.out + ((static_cast<int64_t>(b) * p.n_q_tok + t) * HQ + g * kGqa + h) * kD;
+      reinterpret_cast<float4*>(dst + 8 * lane)[0] = make_float4(v[0] * 0.0625f, v[1] * 0.0625f, v[2] * 0.0625f, v[3] * 0.0625f);
+      reinterpret_cast<float4*>(dst + 8 * lane)[1] = make_float4(v[4] * 0.0625f, v[5] * 0.0625f, v[6] * 0.0625f, v[7] * 0.0625f);
+      if (p.ws && lane == 0) {
+        dst[256] = mrow[r];
+        dst[257] = fsc[r];
+      }
     }
   } else {
     if (tid == 0) {
@@ -638,6 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // a combine launched as a programmatic dependent may start: every partial is written
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace
@@ -654,14 +703,64 @@ int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int
   p.steps = steps;
   p.seq_len = seq_len;
   p.n_q_tok = n_q_tok;
+  p.splits = 1;
+  p.cells_per_split = seq_len + kTileN;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.out = out;
+  p.ws = nullptr;
   p.status = L.status;
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return K8V4_ECUDA;
-  const dim3 grid((n_q_tok + kTokens - 1) / kTokens, C.H);
+  const dim3 grid((n_q_tok + kTokens - 1) / kTokens, C.H, 1);
   prefill_kernel<<<grid, kThreads, kSmemBytes, L.stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
+}
+
+// Verify on the prefill kernel: the n_q (<= 16) queries of a sequence are the
+// CTA's tokens; the cells are split over CTAs, each writing partial rows that
+// launch_combine merges.
+AttendPlan plan_verify_tc(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
+  AttendPlan pl{};
+  pl.n_q = n_q;
+  pl.n_groups = 1;
+  pl.warps = kThreads / 32;
+  const int tiles = max(1, (max_seq_len + kTileN - 1) / kTileN);
+  // about two CTAs per SM over the grid (one resident at a time), so that the
+  // splits of shorter sequences fill in behind the long ones
+  const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
+  int64_t splits = (2ll * num_sms + pairs - 1) / pairs;
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, std::max(1, tiles / 4)));
+  const int tps = static_cast<int>((tiles + splits - 1) / splits);
+  pl.cells_per_split = kTileN * tps;
+  pl.splits = (tiles + tps - 1) / tps;
+  pl.ws_bytes = static_cast<size_t>(n_seqs) * pl.splits * n_q * C.H * kGqa * 260 * sizeof(float);
+  return pl;
+}
+
+int launch_verify_tc(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q,
+                     const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
+                     float sm_scale, float* out, void* ws) {
+  if (n_seqs == 0) return K8V4_OK;
+  PrefillParams p;
+  p.C = C;
+  p.q = static_cast<const uint16_t*>(q);
+  p.pt = pt;
+  p.max_pages = max_pages;
+  p.steps = steps;
+  p.seq_len = max_seq_len;
+  p.n_q_tok = plan.n_q;
+  p.splits = plan.splits;
+  p.cells_per_split = plan.cells_per_split;
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.out = nullptr;
+  p.ws = static_cast<float*>(ws);
+  p.status = L.status;
+  if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return K8V4_ECUDA;
+  const dim3 grid((plan.n_q + kTokens - 1) / kTokens, C.H, n_seqs * plan.splits);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, L.stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
+  return launch_combine(L, p.ws, plan.splits, n_seqs, plan.n_q, C.H, out);
 }
 
 }  // namespace k8v4

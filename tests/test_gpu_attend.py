@@ -129,17 +129,19 @@ def test_verify_small(n_q):
 
 
 @pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8])
-def test_verify_irregular_steps_p16_fp32(fmt):
-    """Verify over 16-cell pages with fp32 queries and irregular per-query steps
-    (0, 1, a page edge, mid-tile, the whole sequence): three sequences, 7
-    queries each, every row checked."""
+@pytest.mark.parametrize("P,qdt", [(16, "f32"), (64, "bf16")])
+def test_verify_irregular_steps(fmt, P, qdt):
+    """Verify with irregular per-query steps (0, 1, page and tile edges,
+    mid-tile, the whole sequence): three sequences, 7 queries each, every row
+    checked; 16-cell pages with fp32 queries (warp-MMA kernel) and 64-cell pages
+    with bf16 queries (tcgen05 kernel for k8v4)."""
     seed = synth.config_seed(4) + 77
-    P, H, n_q = 16, 2, 7
+    H, n_q = 2, 7
     lens = np.array([1500, 33, 700], np.int32)
     pt, n_pages = synth.interleaved_pool(seed, lens, P)
     ks = [synth.kv_values(seed, synth.T_K, b, int(n), H, 3, "bf16") for b, n in enumerate(lens)]
     vs = [synth.kv_values(seed, synth.T_V, b, int(n), H, 3, "bf16") for b, n in enumerate(lens)]
-    qs = [synth.q_values(seed, b, n_q, H, "f32") for b in range(len(lens))]
+    qs = [synth.q_values(seed, b, n_q, H, qdt) for b in range(len(lens))]
     steps = np.array([[0, 1, 16, 17, 499, 1499, 1500],
                       [33, 0, 1, 31, 32, 16, 15],
                       [700, 699, 64, 65, 0, 2, 350]], np.int32)

@@ -5,9 +5,10 @@
 // unrotated INT8 (ties to even), V is rotated by the 256-point Walsh-Hadamard
 // transform and quantised to Q4_0, and each token is written through the page
 // table.  Unlike the pages' engine (separate q8 and q4 append launches with
-// the unused half folded onto one pool) this is one fused kernel: a pair of
-// warps per (token, KV head), one quantising K, the other rotating V exactly and
-// quantising it, each storing its runs with vector stores.
+// the unused half folded onto one pool) this is one fused kernel: one warp per
+// (token, KV head) loads K and V once, quantises K, rotates V exactly, quantises
+// it, and stores all four runs with vector stores (for short appends a warp pair
+// per (token, head) does the K and the V halves concurrently).
 //
 // The rotation is defined as the correctly rounded fp32 value of the exact
 // (H x) / 16.  The warp computes it with an int64 fixed-point fast Walsh-Hadamard
@@ -282,20 +283,21 @@ template <bool BF16, int FMT>
 __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const int32_t* __restrict__ pt,
                                                              int64_t max_pages, const int64_t* __restrict__ pos,
                                                              int n_seqs, int n_tok, const void* __restrict__ k,
-                                                             const void* __restrict__ v, int* status) {
+                                                             const void* __restrict__ v, int split_kv, int* status) {
   __shared__ float stage[kWarps][kD];
   // a kernel launched after this one as a programmatic dependent (the decode
   // attention) may start its launch now; it waits for this grid's completion
   // (griddepcontrol.wait) before it reads the cache
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // (seq, token, head) per warp, or, for short appends (a decode step's token),
   // (seq, token, head, half): warp pairs split a (token, head) into its K half
   // (int8 quantisation) and its V half (rotation + q4_0), which run concurrently
   const int64_t wi = static_cast<int64_t>(blockIdx.x) * kWarps + w;
   const int64_t total = static_cast<int64_t>(n_seqs) * n_tok * C.H;
-  if (wi >= 2 * total) return;
-  const bool v_half = (wi & 1) != 0;
-  const int64_t item = wi >> 1;                                         // (seq, token, head)
+  if (wi >= (split_kv ? 2 * total : total)) return;
+  const int role = split_kv ? static_cast<int>(wi & 1) : 2;             // 0: K only, 1: V only, 2: both
+  const int64_t item = split_kv ? wi >> 1 : wi;                         // (seq, token, head)
   const int g = static_cast<int>(item % C.H);
   const int64_t it = item / C.H;
   const int b = static_cast<int>(it / n_tok), t = static_cast<int>(it % n_tok);
@@ -310,14 +312,14 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const 
   const int64_t elem = item * kD + 8 * lane;
 
   float x[8];
-  if (!v_half) {
+  if (role != 1) {
     load8<BF16>(k, elem, x);
     uint2 kc;
     const float s = quant_int8_half(x, kc);
     const float s_hi = __shfl_xor_sync(kFull, s, 16);
     *reinterpret_cast<uint2*>(base + r * 256 + 8 * lane) = kc;
     if (lane == 0) *reinterpret_cast<float2*>(base + C.ks_off() + r * 8) = make_float2(s, s_hi);
-    return;
+    if (role == 0) return;
   }
 
   load8<BF16>(v, elem, x);
@@ -408,16 +410,19 @@ int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_
                   const int64_t* pos, int n_tok, const void* k, const void* v, int dtype) {
   const int64_t items = static_cast<int64_t>(n_seqs) * n_tok * C.H;
   if (items == 0) return K8V4_OK;
-  const int64_t blocks = (2 * items + kWarps - 1) / kWarps;             // two warps per (token, head)
+  // short appends (up to a few thousand (token, head) items, e.g. a decode
+  // step) take a warp pair per item for latency; long ones a warp per item
+  const int split = items * 2 <= static_cast<int64_t>(L.num_sms) * 16 ? 1 : 0;
+  const int64_t blocks = ((split ? 2 : 1) * items + kWarps - 1) / kWarps;
   if (blocks > 0x7fffffffll) return K8V4_EINVAL;
   const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
   const bool bf = dtype == K8V4_BF16;
   if (C.fmt == K8V4_FORMAT_K8V4) {
-    if (bf) append_kernel<true, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, L.status);
-    else append_kernel<false, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, L.status);
+    if (bf) append_kernel<true, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+    else append_kernel<false, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
   } else {
-    if (bf) append_kernel<true, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, L.status);
-    else append_kernel<false, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, L.status);
+    if (bf) append_kernel<true, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+    else append_kernel<false, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
   }
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
 }

@@ -515,8 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   };
   auto stage_k = [&](int t) {      // (c): convert K(t) and issue QK(t)
     cp_async_wait<0>();            // raw(t) is the most recently committed copy group
-    __syncthreads();
-    const bool ok = __syncthreads_and(ok_tile[t & 1] ? 1 : 0) != 0;
+    const bool ok = __syncthreads_and(ok_tile[t & 1] ? 1 : 0) != 0;   // also: raw(t) visible to all
     valid_bits = ok ? (valid_bits | (1u << (t & 1))) : (valid_bits & ~(1u << (t & 1)));
     convert_k(t & 1);
     fence_async_smem();
@@ -573,11 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
         const float a = ex2_ftz(fmaf(sc[c], my_f, -mu)), b = ex2_ftz(fmaf(sc[c + 1], my_f, -mu));
-        // hi plane: a rounded to 11 significant bits (exact in fp16 in the normal range)
-        const float ah = __uint_as_float((__float_as_uint(a) + 0x1000u) & 0xffffe000u);
-        const float bh = __uint_as_float((__float_as_uint(b) + 0x1000u) & 0xffffe000u);
-        const __half2 h1 = __floats2half2_rn(ah, bh);
-        const __half2 h2 = __floats2half2_rn(a - ah, b - bh);
+        // hi plane: fp16(a); lo plane: fp16 of the exact fp32 residual
+        const __half2 h1 = __floats2half2_rn(a, b);
+        const float2 f1 = __half22float2(h1);
+        const float2 r = __ffma2_rn(f1, make_float2(-1.0f, -1.0f), make_float2(a, b));   // exact
+        const __half2 h2 = __floats2half2_rn(r.x, r.y);
         psum2 = __fadd2_rn(psum2, make_float2(a, b));
         p1v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h1));
         p2v[c >> 1] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));

@@ -43,6 +43,34 @@ def test_prefill_causal_small(n_cells, n_tok):
     assert rel_err(got.reshape(-1, 256), want) <= TOL
 
 
+@pytest.mark.parametrize("P", [128, 256])
+def test_prefill_page_sizes(P):
+    """Pages of 128 and 256 cells (several 64-cell tiles per page), a ragged last
+    page and a ragged last block of 16 tokens."""
+    n_cells, n_tok = 1500, 77
+    w, gpu, ref, pt_d = _build(synth.config_seed(5) + P, n_cells, P=P)
+    q = synth.q_values(w.seed, 9, n_tok, 2, "bf16")
+    got = _prefill(gpu, dev_tensor(q, (n_tok, 16, 256)), pt_d[0], n_cells)
+    assert k8.k8v4_last_device_status() == 0
+    steps = (n_cells - n_tok + 1 + np.arange(n_tok))[None].astype(np.int32)
+    rs, rh, rv = oracle.multi_query_rows(steps, 16)
+    want = ref.attention(w.page_table, rs, rh, rv, q.f32.reshape(-1, 256))
+    assert rel_err(got.reshape(-1, 256), want) <= TOL
+
+
+def test_prefill_rejects_pages_below_a_tile():
+    """16-cell pages cannot hold a 64-cell tile: the call is refused before any
+    launch and the output is untouched."""
+    w, gpu, ref, pt_d = _build(synth.config_seed(5) + 16, 200, P=16)
+    q = synth.q_values(w.seed, 10, 8, 2, "bf16")
+    out = torch.full((8, 16, 256), 7.0, dtype=torch.float32, device="cuda")
+    with pytest.raises(k8.K8V4Error) as e:
+        k8.attn_k8v4_prefill(gpu, dev_tensor(q, (8, 16, 256)), pt_d[0], 200, out)
+    assert e.value.code == k8.EINVAL
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
 def test_prefill_step_arrays():
     """Explicit per-token visible counts in any order, including 0 (zero output)
     and 1 (exactly the first cell's V)."""

@@ -427,6 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     }
   };
   // ---- tensor-core work (one thread issues)
+  // The operand tiles sit at fixed addresses, so their descriptors are built
+  // once; a descriptor of base + off is the base descriptor plus off / 16 (the
+  // 14-bit address field cannot carry: shared addresses stay below 2^18).
+  const uint64_t dq0 = smem_desc(sbase + kQOff, 16, 1024);
+  const uint64_t dk0 = smem_desc(sbase + kKfOff, 16, 1024);
+  const uint64_t dv0 = smem_desc(sbase + kVfOff, 8192, 1024);
   auto issue_qk = [&](int buf) {                  // S[buf]_h = Q_h Kf_h^T, fresh accumulators
     tc_fence_after();
     constexpr uint32_t idS = idesc_f16(128, 64, false, false);
@@ -436,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       for (int kk = 0; kk < 8; ++kk) {
         const int chunk = 2 * h + (kk >> 2);
         const uint32_t off = (kk & 3) * 32;
-        const uint64_t a = smem_desc(sbase + kQOff + chunk * 16384 + off, 16, 1024);
-        const uint64_t b = smem_desc(sbase + kKfOff + chunk * 8192 + off, 16, 1024);
+        const uint64_t a = dq0 + ((chunk * 16384 + off) >> 4);
+        const uint64_t b = dk0 + ((chunk * 8192 + off) >> 4);
         mma_f16(tmem + kSBuf * buf + (h ? kS1Col : kS0Col), a, b, idS, kk > 0 ? 1u : 0u);
       }
     }
@@ -449,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     const uint32_t pb = tmem + kSBuf * buf;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {               // 16 cells = 8 TMEM columns of fp16 pairs
-      const uint64_t v1 = smem_desc(sbase + kVfOff + kk * 2048, 8192, 1024);
-      const uint64_t v2 = smem_desc(sbase + kVfOff + 32768 + kk * 2048, 8192, 1024);
+      const uint64_t v1 = dv0 + ((kk * 2048) >> 4);
+      const uint64_t v2 = dv0 + ((32768 + kk * 2048) >> 4);
       mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v1, idO, (kk > 0 || !fresh) ? 1u : 0u);
       mma_f16_ta(tmem + kOCol, pb + kP1Col + 8 * kk, v2, idO, 1u);
       mma_f16_ta(tmem + kOCol, pb + kP2Col + 8 * kk, v1, idO, 1u);

@@ -5,7 +5,7 @@ cells, 2 KV heads x 256, 16 query heads (GQA 8), page size 64, shuffled page
 table, bf16 K/V/q N(0,1) with 3 outlier channels per head x20.  One step is the
 engine's decode step: append the newest token's K/V (quantise + paged write)
 and run split-K decode attention over all 237,568 cells (partials + combine with
-the inverse Walsh-Hadamard transform).  Two cache replicas alternate between
+the inverse Walsh-Hadamard transform), issued as one attn_k8v4_decode_step call.  Two cache replicas alternate between
 steps (388 MB > L2), so every step streams its cache from HBM.
 
 Metric: decode-attention GB/s over 816 B/cell (and cells/s); the same line also
@@ -356,9 +356,8 @@ def main():
 
     # ---- decode step inputs
     q = torch.from_numpy(w.q.dev.view(np.int16)).view(torch.bfloat16).reshape(1, HQ, 256).to(dev)
-    pos_last = torch.full((1,), N_CELLS - 1, dtype=torch.int64, device=dev)
-    k_new = kd[:, N_CELLS - 1:].contiguous()
-    v_new = vd[:, N_CELLS - 1:].contiguous()
+    k_new = kd[0, N_CELLS - 1:].contiguous()          # [1 sequence][H][256]: the newest token
+    v_new = vd[0, N_CELLS - 1:].contiguous()
     lens = torch.full((1,), N_CELLS, dtype=torch.int32, device=dev)
     out = torch.empty(1, HQ, 256, dtype=torch.float32, device=dev)
     wsp = k8.workspace(caches[0], 1, 1, N_CELLS, device=dev)
@@ -368,9 +367,8 @@ def main():
         torch.cuda.empty_cache()
 
     def step(i):
-        c = caches[i % n_rep]
-        k8.kv_append_k8v4(c, pt, pos_last, k_new, v_new)
-        k8.attn_k8v4_decode(c, q, pt, lens, N_CELLS, out, wsp)
+        # one call: the CTA whose cells hold the newest one appends it, then all attend
+        k8.attn_k8v4_decode_step(caches[i % n_rep], q, k_new, v_new, pt, lens, N_CELLS, out, wsp)
 
     for i in range(args.warmup):
         step(i)
@@ -440,9 +438,7 @@ def main():
         q_s.copy_(q_h, non_blocking=True)
         kn_s.copy_(kn_h, non_blocking=True)
         vn_s.copy_(vn_h, non_blocking=True)
-        c = caches[i % n_rep]
-        k8.kv_append_k8v4(c, pt, pos_last, kn_s, vn_s)
-        k8.attn_k8v4_decode(c, q_s, pt, lens, N_CELLS, out, wsp)
+        k8.attn_k8v4_decode_step(caches[i % n_rep], q_s, kn_s, vn_s, pt, lens, N_CELLS, out, wsp)
         out_h.copy_(out, non_blocking=True)
 
     for i in range(10):
@@ -472,7 +468,8 @@ def main():
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "storage": "int8 K + q4_0 V, 816 B/cell", "data": "synthetic",
         "config": {"workload": WORKLOAD, "cells": N_CELLS, "page_size": P, "n_kv_heads": H, "n_q_heads": HQ,
-                   "step": "append 1 token + split-K decode attention (partials + combine/inverse WHT)",
+                   "step": "append 1 token + split-K decode attention (partials + combine/inverse WHT), one call "
+                           "(attn_k8v4_decode_step: the CTA holding the newest cell writes it first)",
                    "l2": "inputs larger than L2: two 193.9 MB cache replicas alternate (387.7 MB > 135.5 MB L2)",
                    "parallelism": f"replicas x{world}"},
         "cells_per_s": cells_per_s,
@@ -494,7 +491,7 @@ def main():
                     "frac_bf16_sustained": prefill["tflops"] / bf16_sus,
                     "peak_note": "bf16 dense cuBLAS peaks from MEASURED_PEAKS.json (burst and sustained); the "
                                  "kernel's fp16 operands run at the same nominal rate"},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
         "clocks": clk.summary(),
     }
 

@@ -136,6 +136,26 @@ int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, co
                      int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
                      float sm_scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Fused decode step: append each sequence's newest token, then decode.
+ * Equivalent to kv_append_k8v4 of one token at position seq_lens[b] - 1 for
+ * every sequence followed by attn_k8v4_decode over seq_lens[b] cells (the
+ * engine's decode step: the PR's append of the token's K (int8) and rotated V
+ * (q4_0), "What"/"How", then its mode-3 attention, "Tests"); the cache bytes
+ * written and the output are the same as those two calls'.  The CTA of the
+ * split-K grid whose cell range holds the newest cell writes it before any of
+ * its warps reads that cell, so the append costs no separate launch.
+ *   k_new, v_new: [n_seqs][H][256] of kv_dtype (K8V4_F32 or K8V4_BF16),
+ *             16-byte aligned, device memory.
+ *   seq_lens: int32 [n_seqs] (device), each in [1, max_seq_len] for a sequence
+ *             that gets a token (0: no token, zero output); a length past
+ *             max_seq_len is clipped, recorded, and its token not written.
+ *   Every other argument as attn_k8v4_decode.  A page id of the newest cell
+ *   that is out of range is recorded (K8V4_ERANGE) and the token skipped. */
+int attn_k8v4_decode_step(const k8v4_cache* cache, const void* q, int32_t q_dtype, const void* k_new,
+                          const void* v_new, int32_t kv_dtype, const int32_t* page_table, int64_t max_pages,
+                          const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len, float sm_scale,
+                          float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Decode attention that allocates nothing and takes no workspace.  The pages
  * have no counterpart to this call; it exists for callers that cannot allocate
  * device memory: a host with no device allocator of its own (a plain C program

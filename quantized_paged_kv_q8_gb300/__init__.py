@@ -60,6 +60,7 @@ def lib():
             "attn_k8v4_workspace_bytes": ([C, I32, I32, I32], SZ),
             "attn_k8v4_decode": ([C, P, I32, P, I64, P, I32, I32, F, P, P, SZ, P], ctypes.c_int),
             "attn_k8v4_decode_noalloc": ([C, P, I32, P, I64, P, I32, I32, F, P, P], ctypes.c_int),
+            "attn_k8v4_decode_step": ([C, P, I32, P, P, I32, P, I64, P, I32, I32, F, P, P, SZ, P], ctypes.c_int),
             "attn_k8v4_verify": ([C, P, I32, P, I64, P, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
             "attn_k8v4_prefill": ([C, P, I32, P, I64, I32, I32, P, F, P, P], ctypes.c_int),
             "kv_dequant_k8v4": ([C, P, I64, I64, I64, P, P, P, P], ctypes.c_int),
@@ -74,7 +75,8 @@ def lib():
 
 
 EXPORTED = ("k8v4_bytes_per_cell", "k8v4_status_string", "k8v4_device_check", "kv_append_k8v4",
-            "attn_k8v4_workspace_bytes", "attn_k8v4_decode", "attn_k8v4_decode_noalloc", "attn_k8v4_verify",
+            "attn_k8v4_workspace_bytes", "attn_k8v4_decode", "attn_k8v4_decode_noalloc", "attn_k8v4_decode_step",
+            "attn_k8v4_verify",
             "attn_k8v4_prefill",
             "kv_dequant_k8v4", "k8v4_last_device_status")
 
@@ -167,6 +169,20 @@ def attn_k8v4_decode(cache: PagedCache, q: torch.Tensor, page_table: torch.Tenso
                                 _ptr(seq_lens), q.shape[0], max_seq_len, sm_scale, _ptr(out), _ptr(ws),
                                 ws.numel(), _stream(stream))
     _check(rc, "attn_k8v4_decode")
+    return out
+
+
+def attn_k8v4_decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                          page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, out: torch.Tensor,
+                          ws: torch.Tensor, sm_scale: float = 1.0 / 16.0, stream=None) -> torch.Tensor:
+    """Append each sequence's newest token (k_new, v_new: [n_seqs, H, 256], at cell
+    seq_lens[b] - 1) and decode over seq_lens[b] cells, in one call."""
+    assert q.is_contiguous() and out.is_contiguous() and out.dtype == torch.float32
+    assert k_new.is_contiguous() and v_new.is_contiguous() and k_new.dtype == v_new.dtype
+    rc = lib().attn_k8v4_decode_step(cache.ref(), _ptr(q), _dtype(q), _ptr(k_new), _ptr(v_new), _dtype(k_new),
+                                     _ptr(page_table), page_table.shape[-1], _ptr(seq_lens), q.shape[0],
+                                     max_seq_len, sm_scale, _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "attn_k8v4_decode_step")
     return out
 
 

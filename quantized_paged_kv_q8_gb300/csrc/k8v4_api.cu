@@ -145,7 +145,8 @@ size_t attn_k8v4_workspace_bytes(const k8v4_cache* cache, int32_t n_seqs, int32_
 
 static int attend_common(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                          int64_t max_pages, const int32_t* steps, int32_t n_seqs, int32_t n_q, int32_t max_seq_len,
-                         float sm_scale, float* out, void* ws, size_t ws_bytes, void* stream) {
+                         float sm_scale, float* out, void* ws, size_t ws_bytes, void* stream,
+                         const void* k_new = nullptr, const void* v_new = nullptr, int32_t kv_dtype = K8V4_BF16) {
   CacheView C;
   int rc = view_of(cache, &C);
   if (rc) return rc;
@@ -161,7 +162,8 @@ static int attend_common(const k8v4_cache* cache, const void* q, int32_t q_dtype
   if ((rc = make_launch(stream, &L))) return rc;
   const AttendPlan plan = plan_attend(C, n_seqs, n_q, max_seq_len, L.num_sms);
   if (ws_bytes < plan.ws_bytes) return K8V4_ENOSPACE;
-  return launch_attend(L, C, plan, q, q_dtype, page_table, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
+  return launch_attend(L, C, plan, q, q_dtype, page_table, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws,
+                       k_new, v_new, kv_dtype);
 }
 
 int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
@@ -169,6 +171,19 @@ int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, co
                      float* out, void* workspace, size_t workspace_bytes, void* stream) {
   return attend_common(cache, q, q_dtype, page_table, max_pages, seq_lens, n_seqs, 1, max_seq_len, sm_scale, out,
                        workspace, workspace_bytes, stream);
+}
+
+int attn_k8v4_decode_step(const k8v4_cache* cache, const void* q, int32_t q_dtype, const void* k_new,
+                          const void* v_new, int32_t kv_dtype, const int32_t* page_table, int64_t max_pages,
+                          const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len, float sm_scale,
+                          float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_seqs > 0) {
+    if (!k_new || !v_new) return K8V4_EINVAL;
+    if (kv_dtype != K8V4_F32 && kv_dtype != K8V4_BF16) return K8V4_EINVAL;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return K8V4_EALIGN;
+  }
+  return attend_common(cache, q, q_dtype, page_table, max_pages, seq_lens, n_seqs, 1, max_seq_len, sm_scale, out,
+                       workspace, workspace_bytes, stream, k_new, v_new, kv_dtype);
 }
 
 int attn_k8v4_verify(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,

@@ -23,7 +23,7 @@
 // Walsh-Hadamard transform (out = (H/16) o) for the k8v4 format.
 #include <algorithm>
 
-#include "k8v4_common.cuh"
+#include "k8v4_quant.cuh"
 
 namespace k8v4 {
 namespace {
@@ -66,6 +66,9 @@ struct AttendParams {
   float sm_scale_log2;
   float* ws;
   int* status;
+  const void* k_new;       // fused decode step: the new token's K and V [n_seqs][H][256], else null
+  const void* v_new;
+  int kv_bf16;
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -218,6 +221,35 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
   const int c_end = min(c_stop, n_max);
   const int n_tiles = c_end > c_begin ? (c_end - c_begin + 15) >> 4 : 0;
   const int lim = min(n_vis, c_stop);       // this query's cells in this split end here
+
+  // ---- fused decode step: the CTA whose cells include the newest one (n_vis - 1)
+  // appends the new token's K and V there before any warp stages a tile
+  if (NQ1 && p.k_new != nullptr) {
+    const int cell = n_vis - 1;
+    const int raw_len = p.steps[b];
+    if (cell >= c_begin && cell < c_stop && raw_len == n_vis) {   // skipped for a clipped length
+      if (warp < 2) {
+        const int64_t pidx = cell / C.P;
+        const int64_t page = pidx < p.max_pages ? p.pt[static_cast<int64_t>(b) * p.max_pages + pidx] : -1;
+        if (page >= 0 && page < C.n_pages) {
+          uint8_t* base = C.pages + page * C.page_bytes;
+          const int64_t r = static_cast<int64_t>(cell % C.P) * C.H + g;
+          const int64_t elem = (static_cast<int64_t>(b) * C.H + g) * kD + 8 * lane;
+          if (warp == 0) {
+            if (p.kv_bf16) append_k_row<true>(C, base, r, p.k_new, elem, lane);
+            else append_k_row<false>(C, base, r, p.k_new, elem, lane);
+          } else {
+            float* xs = reinterpret_cast<float*>(smem);    // the rotation's slow-path staging (pipeline not started)
+            if (p.kv_bf16) append_v_row<true, FMT>(C, base, r, p.v_new, elem, lane, xs);
+            else append_v_row<false, FMT>(C, base, r, p.v_new, elem, lane, xs);
+          }
+        } else if (warp == 0 && lane == 0) {
+          record_status(p.status, K8V4_ERANGE);
+        }
+      }
+      __syncthreads();                      // the new cell's bytes are visible to every warp's copies
+    }
+  }
 
   // ---- q fragments (B operand of QK^T): lane holds head r0, dims 64i + 16c + 4j + e
   uint32_t qf[16][2];
@@ -677,7 +709,7 @@ AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len,
 
 int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
-                  float sm_scale, float* out, void* ws) {
+                  float sm_scale, float* out, void* ws, const void* k_new, const void* v_new, int kv_dtype) {
   if (n_seqs == 0) return K8V4_OK;
   if (plan.n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) {
     if (q_dtype == K8V4_BF16 && C.P % 64 == 0)
@@ -700,6 +732,9 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.ws = static_cast<float*>(ws);
   p.status = L.status;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.kv_bf16 = kv_dtype == K8V4_BF16 ? 1 : 0;
   const bool f32 = q_dtype == K8V4_F32, one = plan.n_q == 1;
   if (C.fmt == K8V4_FORMAT_K8V4) {
     if (f32) return one ? launch_impl<K8V4_FORMAT_K8V4, true, true>(L, p, plan, out)

@@ -89,9 +89,12 @@ struct AttendPlan {
   size_t ws_bytes;
 };
 AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms);
+// k_new / v_new (n_q = 1 only): append each sequence's newest token (cell
+// steps[b] - 1) from them before attending -- the fused decode step
 int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
-                  float sm_scale, float* out, void* ws);
+                  float sm_scale, float* out, void* ws, const void* k_new = nullptr, const void* v_new = nullptr,
+                  int kv_dtype = K8V4_BF16);
 AttendPlan plan_verify(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms);
 int launch_verify(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,

@@ -181,11 +181,26 @@ __device__ void rotate_exact(float x[8], int lane, float* xs) {
         v[r] = upper ? t - v[r] : v[r] + t;
       }
     }
+    // RN(s * 2^(lo - 4)): the correctly rounded int64 -> fp32 conversion, then an
+    // exact power-of-two scaling by the exponent field while the result stays
+    // normal (or overflows to infinity, as the direct rounding would); a result
+    // in the subnormal range takes the direct rounding (fewer than 24 bits)
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const long long s = v[r];
-      const unsigned long long mag = s < 0 ? 0ull - static_cast<unsigned long long>(s) : static_cast<unsigned long long>(s);
-      x[r] = round_u64(mag, lo - 4, false, s < 0);
+      const float f = __ll2float_rn(s);
+      const uint32_t fb = __float_as_uint(f);
+      const int ef = static_cast<int>((fb >> 23) & 0xffu) + lo - 4;
+      if (s == 0) {
+        x[r] = 0.0f;
+      } else if (ef >= 255) {
+        x[r] = __uint_as_float((fb & 0x80000000u) | 0x7f800000u);
+      } else if (ef >= 1) {
+        x[r] = __uint_as_float((fb & 0x807fffffu) | (static_cast<uint32_t>(ef) << 23));
+      } else {
+        const unsigned long long mag = s < 0 ? 0ull - static_cast<unsigned long long>(s) : static_cast<unsigned long long>(s);
+        x[r] = round_u64(mag, lo - 4, false, s < 0);
+      }
     }
     return;
   }

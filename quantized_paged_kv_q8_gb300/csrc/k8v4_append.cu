@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const 
                                                              int64_t max_pages, const int64_t* __restrict__ pos,
                                                              int n_seqs, int n_tok, const void* __restrict__ k,
                                                              const void* __restrict__ v, int split_kv, int* status) {
-  __shared__ float stage[kWarps][kD];
+  __shared__ long long stage[kWarps][kRotScratch];
   // a kernel launched after this one as a programmatic dependent (the decode
   // attention) may start its launch now; it waits for this grid's completion
   // (griddepcontrol.wait) before it reads the cache
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(CacheView C, const
                                                               int64_t max_pages, int64_t start, int64_t n_cells,
                                                               float* __restrict__ k_out, float* __restrict__ v_rot_out,
                                                               float* __restrict__ v_out, int* status) {
-  __shared__ float stage[kWarps][kD];
+  __shared__ long long stage[kWarps][kRotScratch];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarps + w;   // (cell, head)
   if (item >= n_cells * C.H) return;

@@ -239,9 +239,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
             if (p.kv_bf16) append_k_row<true>(C, base, r, p.k_new, elem, lane);
             else append_k_row<false>(C, base, r, p.k_new, elem, lane);
           } else {
-            float* xs = reinterpret_cast<float*>(smem);    // the rotation's slow-path staging (pipeline not started)
-            if (p.kv_bf16) append_v_row<true, FMT>(C, base, r, p.v_new, elem, lane, xs);
-            else append_v_row<false, FMT>(C, base, r, p.v_new, elem, lane, xs);
+            long long* ts = reinterpret_cast<long long*>(smem);   // the rotation's scratch (pipeline not started)
+            if (p.kv_bf16) append_v_row<true, FMT>(C, base, r, p.v_new, elem, lane, ts);
+            else append_v_row<false, FMT>(C, base, r, p.v_new, elem, lane, ts);
           }
         } else if (warp == 0 && lane == 0) {
           record_status(p.status, K8V4_ERANGE);

@@ -123,8 +123,11 @@ __device__ float exact_rot_elem(const float* xs, int i) {
 }
 
 // Exact rotation of the 256-vector held 8 per lane (element 8 * lane + r).
-// `xs` is this warp's 256-float staging area for the slow path.
-__device__ void rotate_exact(float x[8], int lane, float* xs) {
+// `ts` is this warp's shared scratch of kRotScratch int64 (the fast path's
+// re-dealing; its first 1 KB also stages the floats of the slow path).
+constexpr int kRotScratch = 256 + 32;
+__device__ void rotate_exact(float x[8], int lane, long long* ts) {
+  float* xs = reinterpret_cast<float*>(ts);
   uint32_t M[8];
   int E[8];
   int lo = 1 << 30, hi = -(1 << 30);
@@ -162,25 +165,51 @@ __device__ void rotate_exact(float x[8], int lane, float* xs) {
       const long long a = M[r] ? static_cast<long long>(static_cast<unsigned long long>(M[r]) << (E[r] - lo)) : 0ll;
       v[r] = (__float_as_uint(x[r]) >> 31) ? -a : a;
     }
+    // The eight butterfly stages (one per index bit, in any order) all run
+    // in-lane: the warp re-deals the 256 sums through shared memory so that the
+    // three register bits r cover index bits {0,1,2}, then {3,4,7}, then {5,6}:
+    //   layout 1: i = 8 lane + r
+    //   layout 2: i = (lane & 7) | (r & 3) << 3 | (lane >> 3) << 5 | (r >> 2) << 7
+    //   layout 3: i = (r >> 2) | (lane & 15) << 1 | (r & 3) << 5 | (lane >> 4) << 7
+    // Element i sits at ts[i + i / 8] (one pad slot per eight spreads the banks).
+    auto stages = [&](int nbits) {
 #pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
+      for (int h = 1; h < 8; h <<= 1) {
+        if (h >= (1 << nbits)) break;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if (r & h) continue;
-        const long long a = v[r], b = v[r + h];
-        v[r] = a + b;
-        v[r + h] = a - b;
+        for (int r = 0; r < 8; ++r) {
+          if (r & h) continue;
+          const long long a = v[r], b = v[r + h];
+          v[r] = a + b;
+          v[r + h] = a - b;
+        }
       }
-    }
+    };
+    auto pos = [](int i) { return i + (i >> 3); };
+    const int l1 = pos(8 * lane);
+    const int l2 = pos((lane & 7) | ((lane >> 3) << 5));
+    const int l3 = pos(((lane & 15) << 1) | ((lane >> 4) << 7));
+    stages(3);
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const bool upper = (lane & m) != 0;  // holds index i + 8m of the pair
+    for (int r = 0; r < 8; ++r) ts[l1 + r] = v[r];
+    __syncwarp();
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const long long t = __shfl_xor_sync(kQFull, v[r], m);
-        v[r] = upper ? t - v[r] : v[r] + t;
-      }
-    }
+    for (int r = 0; r < 8; ++r) v[r] = ts[l2 + pos(((r & 3) << 3) | ((r >> 2) << 7))];
+    stages(3);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) ts[l2 + pos(((r & 3) << 3) | ((r >> 2) << 7))] = v[r];
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) v[r] = ts[l3 + pos((r >> 2) | ((r & 3) << 5))];
+    stages(2);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) ts[l3 + pos((r >> 2) | ((r & 3) << 5))] = v[r];
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) v[r] = ts[l1 + r];
+    __syncwarp();
     // RN(s * 2^(lo - 4)): the correctly rounded int64 -> fp32 conversion, then an
     // exact power-of-two scaling by the exponent field while the result stays
     // normal (or overflows to infinity, as the direct rounding would); a result
@@ -299,15 +328,15 @@ __device__ __forceinline__ void append_k_row(const CacheView& C, uint8_t* base, 
   *reinterpret_cast<uint2*>(base + r * 256 + 8 * lane) = kc;
   if (lane == 0) *reinterpret_cast<float2*>(base + C.ks_off() + r * 8) = make_float2(s, s_hi);
 }
-// V row: rotated q4_0 (k8v4) or int8 (the INT8 comparison format); xs is 256
-// floats of this warp's shared memory for the rotation's slow path
+// V row: rotated q4_0 (k8v4) or int8 (the INT8 comparison format); ts is this
+// warp's kRotScratch int64 of shared scratch for the rotation
 template <bool BF16, int FMT>
 __device__ __forceinline__ void append_v_row(const CacheView& C, uint8_t* base, int64_t r, const void* v, int64_t elem,
-                                             int lane, float* xs) {
+                                             int lane, long long* ts) {
   float x[8];
   load8<BF16>(v, elem, x);
   if (FMT == K8V4_FORMAT_K8V4) {
-    rotate_exact(x, lane, xs);
+    rotate_exact(x, lane, ts);
     quant_q4_store(x, lane, base + C.v_off() + r * 128, base + C.vs_off() + r * 16);
   } else {
     uint2 vc;

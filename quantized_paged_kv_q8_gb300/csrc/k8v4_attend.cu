@@ -1,6 +1,8 @@
-// Split-K flash-decode attention over the k8v4 (or INT8) paged cache, for decode
-// (one query per sequence) and verify (n_q queries per sequence with per-query
-// step arrays): the fused "mode 3" attention of the hybrid-KV pull request
+// Split-K flash-decode attention over the k8v4 (or INT8) paged cache: decode
+// (one query per sequence), the fused decode step (append the newest token, then
+// decode), and verify over the INT8 comparison format (n_q queries per sequence
+// with per-query step arrays; k8v4 verify runs in k8v4_prefill.cu or
+// k8v4_verify.cu).  The fused "mode 3" attention of the hybrid-KV pull request
 // ("How": the K loader takes the int8 branch, the V loop the q4 branch, q is not
 // rotated and the output is rotated back; "Tests": step and batched forms with
 // per-query step arrays).
@@ -18,9 +20,11 @@
 //   PV:   A = V codes (16 rotated dims x 16 cells, nibble -> bf16 exactly via
 //         ldmatrix.trans), B = p * d per 32-lane block, split into three bf16
 //         terms (24 significant bits), accumulated in fp32 in rotated space.
-// Online softmax in the log2 domain.  Each CTA writes one partial (m, l, o) per
-// query row; a combine kernel merges the splits and applies the inverse
-// Walsh-Hadamard transform (out = (H/16) o) for the k8v4 format.
+// Online softmax in the log2 domain.  Each CTA merges its warps and writes one
+// partial (m, l, o) per query row, o already rotated back (out = (H/16) o is
+// linear, so it commutes with the merge); the combine (k8v4_combine.cu) merges
+// the splits.  In the fused decode step the CTA whose cells hold the newest one
+// first writes that token (k8v4_quant.cuh row routines), then stages its tiles.
 #include <algorithm>
 
 #include "k8v4_quant.cuh"
@@ -737,10 +741,9 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
   p.kv_bf16 = kv_dtype == K8V4_BF16 ? 1 : 0;
   const bool f32 = q_dtype == K8V4_F32, one = plan.n_q == 1;
   if (C.fmt == K8V4_FORMAT_K8V4) {
-    if (f32) return one ? launch_impl<K8V4_FORMAT_K8V4, true, true>(L, p, plan, out)
-                        : launch_impl<K8V4_FORMAT_K8V4, true, false>(L, p, plan, out);
-    return one ? launch_impl<K8V4_FORMAT_K8V4, false, true>(L, p, plan, out)
-               : launch_impl<K8V4_FORMAT_K8V4, false, false>(L, p, plan, out);
+    // k8v4 with n_q > 1 left above; here n_q == 1
+    return f32 ? launch_impl<K8V4_FORMAT_K8V4, true, true>(L, p, plan, out)
+               : launch_impl<K8V4_FORMAT_K8V4, false, true>(L, p, plan, out);
   }
   if (f32) return one ? launch_impl<K8V4_FORMAT_INT8, true, true>(L, p, plan, out)
                       : launch_impl<K8V4_FORMAT_INT8, true, false>(L, p, plan, out);

@@ -93,3 +93,29 @@ def test_decode_step_bad_page_is_reported():
     changed = np.nonzero(gpu_b.pages.cpu().numpy() != before.cpu().numpy())[0]
     page_bytes = 64 * 816
     assert len(changed) > 0 and set((changed // page_bytes).tolist()) == {int(pt[1, (700 - 1) // 64])}
+
+
+def test_decode_step_config3_full():
+    """The bench's step at full size: 237,567 cells in the cache, the step appends
+    cell 237,567 and attends over all 237,568; every row against the oracle and
+    the cache bytes equal to the oracle's."""
+    n = 237568
+    w = synth.config3(n, seed=synth.config_seed(3))
+    gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv)
+    pt_d = torch.from_numpy(w.page_table).cuda()
+    k8.kv_append_k8v4(gpu, pt_d, torch.zeros(1, dtype=torch.int64).cuda(),
+                      dev_tensor(synth.Tensor(w.k.f32[None, :n - 1], "bf16")),
+                      dev_tensor(synth.Tensor(w.v.f32[None, :n - 1], "bf16")))
+    ref.append(w.page_table, w.pos, w.k.f32[None], w.v.f32[None])
+    out = torch.empty(1, 16, 256, dtype=torch.float32, device="cuda")
+    ws = k8.workspace(gpu, 1, 1, n)
+    k_new = dev_tensor(synth.Tensor(w.k.f32[n - 1:], "bf16"), (1, 2, 256))
+    v_new = dev_tensor(synth.Tensor(w.v.f32[n - 1:], "bf16"), (1, 2, 256))
+    k8.attn_k8v4_decode_step(gpu, dev_tensor(w.q, (1, 16, 256)), k_new, v_new, pt_d,
+                             torch.from_numpy(w.seq_lens).cuda(), n, out, ws)
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    assert np.array_equal(gpu.pages.cpu().numpy(), ref.buf)
+    rs, rh, rv = oracle.decode_rows(1, 16, w.seq_lens)
+    want = ref.attention(w.page_table, rs, rh, rv, w.q.f32.reshape(-1, 256))
+    assert rel_err(out.cpu().numpy().reshape(-1, 256), want) <= TOL

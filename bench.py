@@ -244,6 +244,49 @@ def measure_verify(args, dev, reps: int = 20):
             "gbs": CELL_BYTES * cells / (ms / 1e3) / 1e9, "cells_per_s": cells / (ms / 1e3)}
 
 
+def measure_batched_step(args, dev, n_seqs: int = 32, n_cells: int = 8192, reps: int = 200):
+    """The engine's batched decode shape: n_seqs sequences of n_cells cells each,
+    pages interleaved in one pool; one attn_k8v4_decode_step call appends every
+    sequence's newest token and decodes all of them.  Two cache replicas
+    alternate (2 x 214 MB > L2).  GB/s over 816 B/cell of the cells read."""
+    import torch
+    import quantized_paged_kv_q8_gb300 as k8
+    import synth
+    seed = synth.config_seed(3) + 1000
+    lens = np.full(n_seqs, n_cells, np.int32)
+    pt_np, n_pages = synth.interleaved_pool(seed, lens, P)
+    pt = torch.from_numpy(pt_np).to(dev)
+    caches = [k8.PagedCache(n_pages, P, H, device=dev) for _ in range(2)]
+    for b in range(n_seqs):
+        k = synth.kv_values(seed, synth.T_K, b, n_cells, H, 3, "bf16")
+        v = synth.kv_values(seed, synth.T_V, b, n_cells, H, 3, "bf16")
+        kd = torch.from_numpy(k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, n_cells, H, 256).to(dev)
+        vd = torch.from_numpy(v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, n_cells, H, 256).to(dev)
+        for c in caches:
+            k8.kv_append_k8v4(c, pt[b:b + 1], torch.zeros(1, dtype=torch.int64, device=dev), kd, vd)
+    qv = synth.q_values(seed, 0, n_seqs, H, "bf16")
+    q = torch.from_numpy(qv.dev.view(np.int16)).view(torch.bfloat16).reshape(n_seqs, HQ, 256).to(dev)
+    knew = torch.randn(n_seqs, H, 256, generator=torch.Generator().manual_seed(seed & 0xffff)).to(torch.bfloat16).to(dev)
+    vnew = torch.randn(n_seqs, H, 256, generator=torch.Generator().manual_seed((seed >> 16) & 0xffff)).to(torch.bfloat16).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    out = torch.empty(n_seqs, HQ, 256, dtype=torch.float32, device=dev)
+    ws = k8.workspace(caches[0], n_seqs, 1, n_cells, device=dev)
+    for i in range(10):
+        k8.attn_k8v4_decode_step(caches[i & 1], q, knew, vnew, pt, lens_d, n_cells, out, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        k8.attn_k8v4_decode_step(caches[i & 1], q, knew, vnew, pt, lens_d, n_cells, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    assert k8.k8v4_last_device_status() == 0
+    cells = n_seqs * n_cells
+    return {"workload": f"decode_step_{n_seqs}seq_x_{n_cells}_cells", "cells": cells, "ms_per_step": ms,
+            "gbs": CELL_BYTES * cells / (ms / 1e3) / 1e9, "cells_per_s": cells / (ms / 1e3)}
+
+
 def measure_prefill(args, dev, chunk: int, reps: int = 3):
     """Config 5: 229,376-cell history, then an append of `chunk` tokens at offset
     229,376 (timed: chunk append cells/s) and causal prefill of the chunk (timed:
@@ -301,7 +344,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="k8v4", choices=["k8v4", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify"],
+    ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify", "batched"],
                     help="lean single-kernel run for ncu (no replicas, INT8 arm, e2e or CPU baseline)")
     ap.add_argument("--chunk", type=int, default=8192, help="prefill chunk length (tokens)")
     args = ap.parse_args()
@@ -324,8 +367,9 @@ def main():
     buildlib.build()
     assert k8.k8v4_device_check() == 0, "libk8v4 needs an sm_103 device"
 
-    if args.profile in ("prefill", "verify"):
-        res = measure_prefill(args, dev, args.chunk) if args.profile == "prefill" else measure_verify(args, dev)
+    if args.profile in ("prefill", "verify", "batched"):
+        res = (measure_prefill(args, dev, args.chunk) if args.profile == "prefill"
+               else measure_verify(args, dev) if args.profile == "verify" else measure_batched_step(args, dev))
         if rank == 0:
             print(json.dumps({"profile": args.profile, **res}), flush=True)
         return
@@ -457,6 +501,7 @@ def main():
     del caches, kd, vd
     torch.cuda.empty_cache()
     verify = measure_verify(args, dev)
+    batched = measure_batched_step(args, dev)
     prefill = measure_prefill(args, dev, 8192)
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
@@ -487,6 +532,7 @@ def main():
         "e2e": {"value": dec_bytes / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "verify": {**verify, "frac_hbm": verify["gbs"] / hbm},
+        "batched_step": {**batched, "frac_hbm": batched["gbs"] / hbm},
         "prefill": {**prefill, "frac_bf16_burst": prefill["tflops"] / bf16,
                     "frac_bf16_sustained": prefill["tflops"] / bf16_sus,
                     "peak_note": "bf16 dense cuBLAS peaks from MEASURED_PEAKS.json (burst and sustained); the "

@@ -701,9 +701,11 @@ AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len,
   const int ctas_per_sm = max(1, min(4, (200 * 1024) / max(stage_bytes, 1)));
   const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
   const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm;
-  int64_t splits = (target + pairs - 1) / pairs;
+  // at most one wave (one CTA per SM slot): a second, partly filled wave of
+  // smaller CTAs measured slower than fewer, longer CTAs (each CTA pays its q
+  // setup, pipeline fill and merge epilogue once)
   const int64_t max_splits = std::max(1, tiles / (2 * pl.n_groups));
-  splits = std::max<int64_t>(1, std::min<int64_t>(splits, max_splits));
+  int64_t splits = std::max<int64_t>(1, std::min<int64_t>(target / pairs, max_splits));
   const int tps = static_cast<int>((tiles + splits - 1) / splits);
   pl.cells_per_split = 16 * tps;
   pl.splits = (tiles + tps - 1) / tps;

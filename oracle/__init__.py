@@ -25,6 +25,7 @@ CFLAGS = ["-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "
           "-Wall", "-Wno-unused-function"]
 
 FMT_INT8 = 1
+FMT_Q4 = 2
 FMT_K8V4 = 3
 D = 256
 GQA = 8

@@ -25,6 +25,13 @@
  *    408 B per (cell, head), 816 B per cell at H = 2.
  *  - int8/int8 comparison format: V quantised like K (unrotated), 528 B per
  *    (cell, head): K codes, K scales, V codes [P][H][256], V scales [P][H][2].
+ *  - q4_0 format (both K and V rotated Q4_0, the "--kv q4_0" format the k8v4
+ *    pull request compares against, 576 B/cell): K is rotated and quantised
+ *    exactly like V; runs K nibbles [P][H][8][16], K scales [P][H][8] fp16,
+ *    V nibbles, V scales: 288 B per (cell, head).  Attention scores use
+ *    q . Khat with Khat = (H/16) Khat_rot; since H/16 is symmetric and
+ *    orthogonal this is (H/16 q) . Khat_rot, which the oracle evaluates (q
+ *    rotated once per row in fp64).
  *  - Attention (fp64): s_j = sm_scale * sum_i q_i Khat_ji over the visible cells,
  *    softmax with max subtraction, o = sum_j p_j Vhat_j, and for k8v4 the output
  *    is brought back from rotated space by out = (H/16) o.  Khat = (float)c * s
@@ -236,11 +243,12 @@ void orc_quant_q4_block(const float* y, uint8_t* nib, uint16_t* d_bits) {
 /* page layout                                                                 */
 /* ------------------------------------------------------------------------- */
 
-enum { ORC_FMT_INT8 = 1, ORC_FMT_K8V4 = 3 };
+enum { ORC_FMT_INT8 = 1, ORC_FMT_Q4 = 2, ORC_FMT_K8V4 = 3 };
 
 int64_t orc_bytes_per_cell_head(int fmt) {
   if (fmt == ORC_FMT_K8V4) return 256 + 8 + 128 + 16;
   if (fmt == ORC_FMT_INT8) return 256 + 8 + 256 + 8;
+  if (fmt == ORC_FMT_Q4) return 128 + 16 + 128 + 16;
   return -1;
 }
 
@@ -260,6 +268,13 @@ static cell_ptrs cell_at(const cache_t* C, int b, int64_t c, int g) {
   int64_t P = C->P, H = C->H, r = slot * H + g;
   uint8_t* base = C->pages + page * P * H * orc_bytes_per_cell_head(C->fmt);
   cell_ptrs p;
+  if (C->fmt == ORC_FMT_Q4) {
+    p.kc = base + r * 128;
+    p.ks = base + 128 * H * P + r * 16;
+    p.vq = base + 144 * H * P + r * 128;
+    p.vs = base + 272 * H * P + r * 16;
+    return p;
+  }
   p.kc = base + r * 256;
   p.ks = base + 256 * H * P + r * 8;
   if (C->fmt == ORC_FMT_K8V4) {
@@ -272,8 +287,36 @@ static cell_ptrs cell_at(const cache_t* C, int b, int64_t c, int g) {
   return p;
 }
 
+/* rotate a row and store it as eight Q4_0 blocks (nibbles + fp16 scales) */
+static void write_rot_q4(const float* x, uint8_t* nib, uint8_t* scales) {
+  float y[D];
+  orc_hadamard_rotate(x, y);
+  uint16_t dv[8];
+  for (int blk = 0; blk < 8; ++blk) orc_quant_q4_block(y + 32 * blk, nib + 16 * blk, &dv[blk]);
+  memcpy(scales, dv, 16);
+}
+
+/* the rotated-space values (q - 8) d of eight stored Q4_0 blocks */
+static void read_q4(const uint8_t* nib, const uint8_t* scales, float* out) {
+  uint16_t dv[8];
+  memcpy(dv, scales, 16);
+  for (int blk = 0; blk < 8; ++blk) {
+    float d = orc_f16_to_f32(dv[blk]);
+    for (int j = 0; j < 16; ++j) {
+      uint8_t byte = nib[16 * blk + j];
+      out[32 * blk + j] = (float)((int)(byte & 15) - 8) * d;
+      out[32 * blk + j + 16] = (float)((int)(byte >> 4) - 8) * d;
+    }
+  }
+}
+
 static void write_cell(const cache_t* C, int b, int64_t c, int g, const float* kx, const float* vx) {
   cell_ptrs p = cell_at(C, b, c, g);
+  if (C->fmt == ORC_FMT_Q4) {
+    write_rot_q4(kx, p.kc, p.ks);
+    write_rot_q4(vx, p.vq, p.vs);
+    return;
+  }
   int8_t codes[D];
   float s[2];
   orc_quant_int8(kx, 128, codes, &s[0]);
@@ -294,9 +337,15 @@ static void write_cell(const cache_t* C, int b, int64_t c, int g, const float* k
   }
 }
 
-/* Khat = (float)c * s;  Vhat = (q - 8) * d (k8v4, rotated space) or c * s (int8). */
+/* Khat = (float)c * s (Khat_rot = (q - 8) * d for q4_0);  Vhat = (q - 8) * d
+ * (k8v4 and q4_0, rotated space) or c * s (int8). */
 static void read_cell(const cache_t* C, int b, int64_t c, int g, float* kh, float* vh) {
   cell_ptrs p = cell_at(C, b, c, g);
+  if (C->fmt == ORC_FMT_Q4) {
+    read_q4(p.kc, p.ks, kh);
+    read_q4(p.vq, p.vs, vh);
+    return;
+  }
   float s[2];
   memcpy(s, p.ks, 8);
   const int8_t* kc = (const int8_t*)p.kc;
@@ -391,8 +440,13 @@ int orc_dequant(const uint8_t* pages, int fmt, int P, int H, const int32_t* pt, 
     for (int g = 0; g < H; ++g) {
       int64_t off = (c * H + g) * D;
       read_cell(&C, b, start + c, g, k_out + off, v_rot_out + off);
+      if (fmt == ORC_FMT_Q4) {             /* K back in the original basis */
+        float kr[D];
+        memcpy(kr, k_out + off, sizeof kr);
+        orc_hadamard_rotate(kr, k_out + off);
+      }
       if (v_out) {
-        if (fmt == ORC_FMT_K8V4) orc_hadamard_rotate(v_rot_out + off, v_out + off);
+        if (fmt != ORC_FMT_INT8) orc_hadamard_rotate(v_rot_out + off, v_out + off);
         else memcpy(v_out + off, v_rot_out + off, D * sizeof(float));
       }
     }
@@ -415,7 +469,17 @@ typedef struct {
 static void attn_row(void* vctx, int64_t r) {
   attn_ctx* a = (attn_ctx*)vctx;
   int b = a->row_seq[r], h = a->row_head[r], n = a->row_vis[r], g = h / GQA;
-  const float* q = a->q + r * D;
+  const float* q32 = a->q + r * D;
+  double q[D];
+  if (a->C.fmt == ORC_FMT_Q4) {          /* (H/16) q: scores against Khat_rot */
+    for (int i = 0; i < D; ++i) {
+      double s = 0.0;
+      for (int j = 0; j < D; ++j) s += hadamard_sign(i, j) * (double)q32[j];
+      q[i] = s / 16.0;
+    }
+  } else {
+    for (int i = 0; i < D; ++i) q[i] = (double)q32[i];
+  }
   double* o = a->out + r * D;
   double* sc = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
   double acc[D];
@@ -425,7 +489,7 @@ static void attn_row(void* vctx, int64_t r) {
   for (int j = 0; j < n; ++j) {
     read_cell(&a->C, b, j, g, kh, vh);
     double dot = 0.0;
-    for (int i = 0; i < D; ++i) dot += (double)q[i] * (double)kh[i];
+    for (int i = 0; i < D; ++i) dot += q[i] * (double)kh[i];
     sc[j] = dot * a->sm_scale;
     if (sc[j] > mx) mx = sc[j];
   }
@@ -456,7 +520,7 @@ int orc_attention(const uint8_t* pages, int fmt, int P, int H, const int32_t* pt
                   int64_t n_rows, const int32_t* row_seq, const int32_t* row_head, const int32_t* row_vis,
                   const float* q, double sm_scale, double* out, int rotate_back, int n_threads) {
   attn_ctx a = {{(uint8_t*)pages, fmt, P, H, pt, max_pages}, row_seq, row_head, row_vis, q, sm_scale, out,
-                rotate_back && fmt == ORC_FMT_K8V4};
+                rotate_back && fmt != ORC_FMT_INT8};
   parallel_for(n_threads, n_rows, attn_row, &a);
   return 0;
 }

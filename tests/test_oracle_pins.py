@@ -262,6 +262,8 @@ def test_q4_error_bounds(orc):
 def test_bytes_per_cell(orc):
     assert 2 * orc.bytes_per_cell_head(orc.FMT_K8V4) == 816
     assert 2 * orc.bytes_per_cell_head(orc.FMT_INT8) == 1056
+    # "816 B per cell vs int8's 1,056 (-23%) and q4_0's 576" (#120, section "What")
+    assert 2 * orc.bytes_per_cell_head(orc.FMT_Q4) == 576
     # 816 = 512 K codes + 16 K scales + 256 V nibbles + 32 V scales
     assert 2 * (256 + 8 + 128 + 16) == 816
 
@@ -446,3 +448,88 @@ def test_tie_cells_round_trip(orc):
     nib, db = orc.quant_q4_block(y[:32])
     codes = np.concatenate([nib & 15, nib >> 4])
     assert codes[:9].tolist() == [0, 10, 12, 8, 15, 6, 8, 10, 0]
+
+
+# ----------------------------------------------------------------------------- q4_0 K+V format
+
+def _q4_runs(buf, page, P, H, slot, g):
+    """Byte runs of (page, slot, head) in the q4_0 format, from the layout
+    K nibbles [P][H][8][16], K scales f16 [P][H][8], V nibbles, V scales."""
+    base = page * P * H * 288
+    r = slot * H + g
+    kq = buf[base + r * 128: base + r * 128 + 128]
+    ks = buf[base + 128 * H * P + r * 16: base + 128 * H * P + r * 16 + 16]
+    vq = buf[base + 144 * H * P + r * 128: base + 144 * H * P + r * 128 + 128]
+    vs = buf[base + 272 * H * P + r * 16: base + 272 * H * P + r * 16 + 16]
+    return kq, ks, vq, vs
+
+
+def _q4_values(nib, scales):
+    """(code - 8) * d of eight blocks: byte j holds codes j (low) and j + 16 (high)."""
+    d = np.frombuffer(scales.tobytes(), np.float16).astype(np.float64)
+    out = np.zeros(D)
+    for b in range(8):
+        for j in range(16):
+            byte = int(nib[16 * b + j])
+            out[32 * b + j] = ((byte & 15) - 8) * d[b]
+            out[32 * b + j + 16] = ((byte >> 4) - 8) * d[b]
+    return out
+
+
+def test_q4_format_quantises_k_like_v(orc):
+    """In the q4_0 format K goes through the same rotation + Q4_0 as V: equal K
+    and V inputs give equal K and V runs, and those equal the V runs the k8v4
+    format writes for the same vector."""
+    rng = np.random.default_rng(31)
+    P, H = 4, 2
+    x = rng.standard_normal((1, 3, H, D)).astype(np.float32)
+    x[..., 9] *= 20
+    pt = np.array([[0]], np.int32)
+    q4 = orc.Cache(1, P, H, orc.FMT_Q4)
+    q4.append(pt, np.array([0]), x, x)
+    k8 = orc.Cache(1, P, H, orc.FMT_K8V4)
+    k8.append(pt, np.array([0]), x, x)
+    for slot in range(3):
+        for g in range(H):
+            kq, ks, vq, vs = _q4_runs(q4.buf, 0, P, H, slot, g)
+            assert np.array_equal(kq, vq) and np.array_equal(ks, vs)
+            r = slot * H + g
+            assert np.array_equal(vq, k8.buf[264 * H * P + r * 128: 264 * H * P + r * 128 + 128])
+            assert np.array_equal(vs, k8.buf[392 * H * P + r * 16: 392 * H * P + r * 16 + 16])
+
+
+def test_q4_format_dequant_and_attention(orc):
+    """Dequantised K of the q4_0 format is the exact inverse rotation of its
+    rotated-space values (decoded here from the raw bytes), and fp64 attention
+    equals torch SDPA over K = (H/16) Khat_rot and V = (H/16) Vhat_rot formed
+    in float64 from those bytes."""
+    import torch
+    cache, pt, n = _small_cache(orc, orc.FMT_Q4)
+    kh, vr, vo = cache.dequant(pt, 0, n)
+    Hs = scipy.linalg.hadamard(D).astype(np.float64)
+    P, H = 8, 2
+    krot = np.zeros((n, H, D))
+    vrot = np.zeros((n, H, D))
+    for c in range(n):
+        for g in range(H):
+            kq, ks, vq, vs = _q4_runs(cache.buf, int(pt[0, c // P]), P, H, c % P, g)
+            krot[c, g] = _q4_values(kq, ks)
+            vrot[c, g] = _q4_values(vq, vs)
+    assert np.array_equal(vr.astype(np.float64), vrot)
+    for c in (0, 5, n - 1):
+        for g in range(H):
+            assert np.array_equal(kh[c, g], orc.rotate(krot[c, g].astype(np.float32)))
+    kd = krot @ Hs.T / 16.0
+    vd = vrot @ Hs.T / 16.0
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal((16, D)).astype(np.float32)
+    for vis in (1, 33, n):
+        rs, rh, rv = orc.decode_rows(1, 16, [vis])
+        got = cache.attention(pt, rs, rh, rv, q)
+        for h in range(16):
+            g = h // 8
+            Q = torch.tensor(q[h], dtype=torch.float64)[None, None, None]
+            K = torch.tensor(kd[:vis, g])[None, None]
+            V = torch.tensor(vd[:vis, g])[None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=1.0 / 16.0)[0, 0, 0].numpy()
+            assert np.max(np.abs(got[h] - ref)) < 1e-11 * max(1.0, np.max(np.abs(ref)))

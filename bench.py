@@ -10,9 +10,9 @@ steps (388 MB > L2), so every step streams its cache from HBM.
 
 Metric: decode-attention GB/s over 816 B/cell (and cells/s); the same line also
 reports append cells/s (bulk append of the whole cache, 2,864 B/cell of
-algorithmic traffic), the INT8/INT8 comparison arm (1,056 B/cell), the roofline
-of the decode call, the end-to-end rate through the C ABI with host buffers, and
-the CPU oracle timed on the host cores.
+algorithmic traffic), the INT8/INT8 (1,056 B/cell) and q4_0 K+V (576 B/cell)
+comparison arms, the roofline of the decode call, the end-to-end rate through
+the C ABI with host buffers, and the CPU oracle timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl k8v4|reference]
 
@@ -40,6 +40,7 @@ H = 2
 HQ = 16
 CELL_BYTES = 816
 CELL_BYTES_INT8 = 1056
+CELL_BYTES_Q4 = 576
 APPEND_BYTES = 2 * H * 256 * 2 + CELL_BYTES      # bf16 K+V in, 816 B out
 METRIC = "k8v4 decode-attn GB/s (% HBM peak) and cells/s @238K ctx; append cells/s"
 WORKLOAD = "decode_237568_cells_2kv_16q_gqa8_P64_bf16"
@@ -454,22 +455,31 @@ def main():
                               "gbs": CELL_BYTES * N_CELLS / (dec_ms / 1e3) / 1e9}), flush=True)
         return
 
-    # ---- INT8/INT8 comparison arm (1,056 B/cell), same workload
-    c8 = [k8.PagedCache(n_pages, P, H, fmt=k8.FORMAT_INT8, device=dev) for _ in range(2)]
-    for c in c8:
-        k8.kv_append_k8v4(c, pt, zero, kd, vd)
-    ws8 = k8.workspace(c8[0], 1, 1, N_CELLS, device=dev)
-    for i in range(20):
-        k8.attn_k8v4_decode(c8[i & 1], q, pt, lens, N_CELLS, out, ws8)
-    K8 = max(20, K // 5)
-    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    b0.record()
-    for i in range(K8):
-        k8.attn_k8v4_decode(c8[i & 1], q, pt, lens, N_CELLS, out, ws8)
-    b1.record()
-    torch.cuda.synchronize()
-    int8_ms = b0.elapsed_time(b1) / K8
-    del c8, ws8
+    # ---- comparison formats on the same workload: INT8/INT8 (1,056 B/cell) and
+    # q4_0 K+V (576 B/cell), decode calls over two alternating replicas
+    def format_arm(fmt, cell_bytes):
+        cs = [k8.PagedCache(n_pages, P, H, fmt=fmt, device=dev) for _ in range(2)]
+        for c in cs:
+            k8.kv_append_k8v4(c, pt, zero, kd, vd)
+        wsf = k8.workspace(cs[0], 1, 1, N_CELLS, device=dev)
+        for i in range(20):
+            k8.attn_k8v4_decode(cs[i & 1], q, pt, lens, N_CELLS, out, wsf)
+        Kf = max(20, K // 5)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record()
+        for i in range(Kf):
+            k8.attn_k8v4_decode(cs[i & 1], q, pt, lens, N_CELLS, out, wsf)
+        b1.record()
+        torch.cuda.synchronize()
+        assert k8.k8v4_last_device_status() == 0
+        ms = b0.elapsed_time(b1) / Kf
+        del cs, wsf
+        torch.cuda.empty_cache()
+        return {"gbs": cell_bytes * N_CELLS / (ms / 1e3) / 1e9, "ms_per_step": ms,
+                "cells_per_s": N_CELLS / (ms / 1e3), "bytes_per_cell": cell_bytes, "k8v4_speedup": ms / dec_ms}
+
+    int8_arm = format_arm(k8.FORMAT_INT8, CELL_BYTES_INT8)
+    q4_arm = format_arm(k8.FORMAT_Q4, CELL_BYTES_Q4)
 
     # ---- end to end through the C ABI with host buffers
     q_h = q.cpu().pin_memory()
@@ -526,9 +536,8 @@ def main():
         "append": {"cells_per_s": N_CELLS / append_s, "gbs": APPEND_BYTES * N_CELLS / append_s / 1e9,
                    "frac": APPEND_BYTES * N_CELLS / append_s / 1e9 / hbm, "bytes_per_cell": APPEND_BYTES,
                    "ms_per_launch": append_s * 1e3, "cells_per_launch": N_CELLS},
-        "int8_arm": {"gbs": CELL_BYTES_INT8 * N_CELLS / (int8_ms / 1e3) / 1e9, "ms_per_step": int8_ms,
-                     "cells_per_s": N_CELLS / (int8_ms / 1e3), "bytes_per_cell": CELL_BYTES_INT8,
-                     "k8v4_speedup": int8_ms / dec_ms},
+        "int8_arm": {**int8_arm, "frac_hbm": int8_arm["gbs"] / hbm},
+        "q4_arm": {**q4_arm, "frac_hbm": q4_arm["gbs"] / hbm},
         "e2e": {"value": dec_bytes / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "verify": {**verify, "frac_hbm": verify["gbs"] / hbm},

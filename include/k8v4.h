@@ -36,6 +36,10 @@
  *   format INT8 (the 1,056 B/cell comparison arm, 528 B per cell and head):
  *     K codes [P][H][256] at 0, K scales [P][H][2] f32 at 256*H*P,
  *     V codes [P][H][256] at 264*H*P, V scales [P][H][2] f32 at 520*H*P.
+ *   format Q4 (the 576 B/cell q4_0 arm, 288 B per cell and head; K and V both
+ *   rotated Q4_0, nibble bytes as for the V of K8V4):
+ *     K nibbles [P][H][8][16] at 0, K scales f16 [P][H][8] at 128*H*P,
+ *     V nibbles [P][H][8][16] at 144*H*P, V scales f16 [P][H][8] at 272*H*P.
  *   Cell c of sequence b lives in page page_table[b * max_pages + c / P],
  *   slot c % P.
  *
@@ -48,6 +52,9 @@
  *     code = clamp(rint_even(y / d) + 8, 0, 15); d == 0 -> codes 8.
  *   Attention: out = softmax(sm_scale * q . Khat) . Vhat, Khat = code * s,
  *     Vhat = (H/16) * ((code - 8) * d); fp32 result.
+ *   Q4 format: K is rotated and quantised exactly as V, Khat = (H/16) *
+ *     ((code - 8) * d); the scores are computed as ((H/16) q) . ((code - 8) * d)
+ *     (H/16 is symmetric and orthogonal, so the two are equal).
  */
 #ifndef K8V4_H
 #define K8V4_H
@@ -73,9 +80,11 @@ typedef enum {
 /* Element type of K/V/q inputs. */
 typedef enum { K8V4_F32 = 0, K8V4_BF16 = 1 } k8v4_dtype;
 
-/* Cache format.  3 matches the pages' number for the hybrid format
- * ("KvFormat gains kKvHybrid = 3"); 1 is the all-INT8 comparison format. */
-typedef enum { K8V4_FORMAT_INT8 = 1, K8V4_FORMAT_K8V4 = 3 } k8v4_format;
+/* Cache format.  3 is the number the streaming PR ("How") gives the hybrid
+ * format's enumerator kKvHybrid; 1 is the all-INT8 comparison format and 2
+ * the all-q4_0 one (the pages give those two no numbers; these are this
+ * library's). */
+typedef enum { K8V4_FORMAT_INT8 = 1, K8V4_FORMAT_Q4 = 2, K8V4_FORMAT_K8V4 = 3 } k8v4_format;
 
 /* Descriptor of a caller-owned paged cache (plain data, no ownership). */
 typedef struct {
@@ -88,8 +97,8 @@ typedef struct {
   int32_t format;     /* k8v4_format */
 } k8v4_cache;
 
-/* Bytes per cell (all H heads) of a format: 816 for K8V4 at H = 2, 1,056 for
- * INT8 at H = 2 ("816 B per cell vs int8's 1,056", the k8v4 PR, "What").
+/* Bytes per cell (all H heads) of a format: 816 for K8V4, 1,056 for INT8 and
+ * 576 for Q4 at H = 2 (the three sizes the k8v4 PR compares in "What").
  * Returns 0 for an unknown format or H outside 1..8. */
 size_t k8v4_bytes_per_cell(int32_t format, int32_t n_kv_heads);
 
@@ -101,7 +110,8 @@ const char* k8v4_status_string(int status);
 int k8v4_device_check(void);
 
 /* Quantise n_tok new tokens per sequence and write them through the page table
- * (the append of the k8v4 PR, "How": K to INT8, V rotated then Q4_0; the
+ * (the append of the k8v4 PR, "How": K to INT8, V rotated then Q4_0 -- in
+ * the Q4 format K is rotated and quantised like V; the
  * per-step decode, verify-window and prompt appends of the streaming PR are all
  * this call with different n_tok).
  *   page_table: int32 [n_seqs][max_pages], physical page ids in [0, n_pages).
@@ -131,7 +141,7 @@ size_t attn_k8v4_workspace_bytes(const k8v4_cache* cache, int32_t n_seqs, int32_
  *   out:      float [n_seqs][8*H][256], the un-rotated attention output.
  *   workspace: >= attn_k8v4_workspace_bytes(cache, n_seqs, 1, max_seq_len)
  *             bytes of device memory, 256-byte aligned.
- * A row with zero visible cells outputs zeros.  Works on both formats. */
+ * A row with zero visible cells outputs zeros.  Works on every format. */
 int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                      int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
                      float sm_scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
@@ -182,7 +192,7 @@ int attn_k8v4_decode_noalloc(const k8v4_cache* cache, const void* q, int32_t q_d
  * the steps are len-4 .. len).
  *   q: [n_seqs][n_q][8*H][256]; out: float [n_seqs][n_q][8*H][256];
  *   step_arrays: int32 [n_seqs][n_q] (device), each in [0, max_seq_len];
- *   1 <= n_q <= 8. */
+ *   1 <= n_q <= 8.  Works on every format. */
 int attn_k8v4_verify(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                      int64_t max_pages, const int32_t* step_arrays, int32_t n_seqs, int32_t n_q,
                      int32_t max_seq_len, float sm_scale, float* out, void* workspace, size_t workspace_bytes,
@@ -201,7 +211,8 @@ int attn_k8v4_prefill(const k8v4_cache* cache, const void* q, int32_t q_dtype, c
 
 /* Dequantise cells [start, start + n_cells) of one sequence, for checking (the
  * PR's gather entry points, "Tests": appends and gathers checked bitwise).
- *   k_out:     float [n_cells][H][256] = code * s
+ *   k_out:     float [n_cells][H][256] = code * s (Q4 format: RN_fp32((H/16)
+ *              ((code - 8) * d)), the exact inverse rotation of the stored K)
  *   v_rot_out: float [n_cells][H][256] = (code - 8) * d (rotated space; for the
  *              INT8 format: code * s, unrotated)
  *   v_out:     NULL or float [n_cells][H][256] = RN_fp32((H/16) v_rot), the

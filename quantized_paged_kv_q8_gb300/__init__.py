@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libk8v4.so")
 
 OK, EINVAL, ERANGE, EALIGN, ECUDA, EDEVICE, ENOSPACE = 0, -1, -2, -3, -4, -5, -6
 F32, BF16 = 0, 1
-FORMAT_INT8, FORMAT_K8V4 = 1, 3
+FORMAT_INT8, FORMAT_Q4, FORMAT_K8V4 = 1, 2, 3
 HEAD_DIM = 256
 GQA = 8
 

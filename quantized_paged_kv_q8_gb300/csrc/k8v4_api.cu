@@ -67,7 +67,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int view_of(const k8v4_cache* c, CacheView* v) {
   if (!c || !c->pages) return K8V4_EINVAL;
-  if (c->format != K8V4_FORMAT_K8V4 && c->format != K8V4_FORMAT_INT8) return K8V4_EINVAL;
+  if (c->format != K8V4_FORMAT_K8V4 && c->format != K8V4_FORMAT_INT8 && c->format != K8V4_FORMAT_Q4)
+    return K8V4_EINVAL;
   if (c->head_dim != kD || c->n_kv_heads < 1 || c->n_kv_heads > 8) return K8V4_EINVAL;
   if (c->page_size < 16 || c->page_size > 4096 || c->page_size % 16) return K8V4_EINVAL;
   if (c->n_pages < 1 || c->n_pages > (int64_t(1) << 40)) return K8V4_EINVAL;
@@ -97,7 +98,7 @@ extern "C" {
 
 size_t k8v4_bytes_per_cell(int32_t format, int32_t n_kv_heads) {
   if (n_kv_heads < 1 || n_kv_heads > 8) return 0;
-  if (format != K8V4_FORMAT_K8V4 && format != K8V4_FORMAT_INT8) return 0;
+  if (format != K8V4_FORMAT_K8V4 && format != K8V4_FORMAT_INT8 && format != K8V4_FORMAT_Q4) return 0;
   return static_cast<size_t>(n_kv_heads) * cell_head_bytes(format);
 }
 

@@ -4,7 +4,8 @@
 // Hadamard-rotated Q4_0 V (816 B/cell)", sections "What" and "How": K stays
 // unrotated INT8 (ties to even), V is rotated by the 256-point Walsh-Hadamard
 // transform and quantised to Q4_0, and each token is written through the page
-// table.  Unlike the pages' engine (separate q8 and q4 append launches with
+// table (in the all-q4_0 comparison format K is rotated and quantised like V).
+// Unlike the pages' engine (separate q8 and q4 append launches with
 // the unused half folded onto one pool) this is one fused kernel: one warp per
 // (token, KV head) loads K and V once, quantises K, rotates V exactly, quantises
 // it, and stores all four runs with vector stores (for short appends a warp pair
@@ -35,7 +36,8 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   // (seq, token, head) per warp, or, for short appends (a decode step's token),
   // (seq, token, head, half): warp pairs split a (token, head) into its K half
-  // (int8 quantisation) and its V half (rotation + q4_0), which run concurrently
+  // (int8 quantisation; rotation + q4_0 in the Q4 format) and its V half
+  // (rotation + q4_0, or int8), which run concurrently
   const int64_t wi = static_cast<int64_t>(blockIdx.x) * kWarps + w;
   const int64_t total = static_cast<int64_t>(n_seqs) * n_tok * C.H;
   if (wi >= (split_kv ? 2 * total : total)) return;
@@ -54,11 +56,27 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const 
   uint8_t* base = C.pages + page * C.page_bytes;
   const int64_t elem = item * kD + 8 * lane;
 
-  if (role != 1) append_k_row<BF16>(C, base, r, k, elem, lane);
+  if (role != 1) append_k_row<BF16, FMT>(C, base, r, k, elem, lane, stage[w]);
   if (role != 0) append_v_row<BF16, FMT>(C, base, r, v, elem, lane, stage[w]);
 }
 
 // ------------------------------------------------------------------ dequant
+// Rotated-space values (code - 8) * d of one q4_0 row, elements 8 * lane + r:
+// block lane / 4; element e of a block is the low nibble of byte e (e < 16) or
+// the high nibble of byte e - 16
+__device__ __forceinline__ void read_q4_row(const uint8_t* nib, const uint8_t* scales, int lane, float x[8]) {
+  const int blk = lane >> 2, e0 = 8 * (lane & 3);
+  const float d = __half2float(*reinterpret_cast<const __half*>(scales + 2 * blk));
+  const uint2 raw = *reinterpret_cast<const uint2*>(nib + 16 * blk + (e0 & 15));
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t word = q < 4 ? raw.x : raw.y;
+    const uint32_t byte = (word >> (8 * (q & 3))) & 0xffu;
+    const int code = e0 < 16 ? static_cast<int>(byte & 0xfu) : static_cast<int>(byte >> 4);
+    x[q] = __fmul_rn(static_cast<float>(code - 8), d);
+  }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(CacheView C, const int32_t* __restrict__ pt,
                                                               int64_t max_pages, int64_t start, int64_t n_cells,
@@ -81,32 +99,26 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(CacheView C, const
   }
   const int64_t r = (cell % C.P) * C.H + g;
   const uint8_t* base = C.pages + page * C.page_bytes;
-  const float2 ks = *reinterpret_cast<const float2*>(base + C.ks_off() + r * 8);
-  const float s = lane < 16 ? ks.x : ks.y;
-  const uint2 kc = *reinterpret_cast<const uint2*>(base + r * 256 + 8 * lane);
   float x[8];
+  if (FMT == K8V4_FORMAT_Q4) {
+    // rotated-space K, then the exact inverse rotation (H/16 is its own inverse)
+    read_q4_row(base + r * 128, base + C.ks_off() + r * 16, lane, x);
+    rotate_exact(x, lane, stage[w]);
+  } else {
+    const float2 ks = *reinterpret_cast<const float2*>(base + C.ks_off() + r * 8);
+    const float s = lane < 16 ? ks.x : ks.y;
+    const uint2 kc = *reinterpret_cast<const uint2*>(base + r * 256 + 8 * lane);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint32_t word = q < 4 ? kc.x : kc.y;
-    const int c = static_cast<int8_t>((word >> (8 * (q & 3))) & 0xffu);
-    x[q] = __fmul_rn(static_cast<float>(c), s);
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t word = q < 4 ? kc.x : kc.y;
+      const int c = static_cast<int8_t>((word >> (8 * (q & 3))) & 0xffu);
+      x[q] = __fmul_rn(static_cast<float>(c), s);
+    }
   }
   reinterpret_cast<float4*>(ko)[0] = make_float4(x[0], x[1], x[2], x[3]);
   reinterpret_cast<float4*>(ko)[1] = make_float4(x[4], x[5], x[6], x[7]);
-  if (FMT == K8V4_FORMAT_K8V4) {
-    // elements 8*lane .. 8*lane+7 of block lane/4; element e of a block is the
-    // low nibble of byte e (e < 16) or the high nibble of byte e - 16
-    const int blk = lane >> 2, e0 = 8 * (lane & 3);
-    const uint8_t* vq = base + C.v_off() + r * 128 + 16 * blk;
-    const float d = __half2float(*reinterpret_cast<const __half*>(base + C.vs_off() + r * 16 + 2 * blk));
-    const uint2 raw = *reinterpret_cast<const uint2*>(vq + (e0 & 15));
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint32_t word = q < 4 ? raw.x : raw.y;
-      const uint32_t byte = (word >> (8 * (q & 3))) & 0xffu;
-      const int code = e0 < 16 ? static_cast<int>(byte & 0xfu) : static_cast<int>(byte >> 4);
-      x[q] = __fmul_rn(static_cast<float>(code - 8), d);
-    }
+  if (FMT != K8V4_FORMAT_INT8) {
+    read_q4_row(base + C.v_off() + r * 128, base + C.vs_off() + r * 16, lane, x);
   } else {
     const float2 vsc = *reinterpret_cast<const float2*>(base + C.vs_off() + r * 8);
     const float sv = lane < 16 ? vsc.x : vsc.y;
@@ -121,7 +133,7 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(CacheView C, const
   reinterpret_cast<float4*>(vr)[0] = make_float4(x[0], x[1], x[2], x[3]);
   reinterpret_cast<float4*>(vr)[1] = make_float4(x[4], x[5], x[6], x[7]);
   if (vo) {
-    if (FMT == K8V4_FORMAT_K8V4) rotate_exact(x, lane, stage[w]);
+    if (FMT != K8V4_FORMAT_INT8) rotate_exact(x, lane, stage[w]);
     reinterpret_cast<float4*>(vo)[0] = make_float4(x[0], x[1], x[2], x[3]);
     reinterpret_cast<float4*>(vo)[1] = make_float4(x[4], x[5], x[6], x[7]);
   }
@@ -143,6 +155,9 @@ int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_
   if (C.fmt == K8V4_FORMAT_K8V4) {
     if (bf) append_kernel<true, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
     else append_kernel<false, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+  } else if (C.fmt == K8V4_FORMAT_Q4) {
+    if (bf) append_kernel<true, K8V4_FORMAT_Q4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+    else append_kernel<false, K8V4_FORMAT_Q4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
   } else {
     if (bf) append_kernel<true, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
     else append_kernel<false, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
@@ -159,6 +174,8 @@ int launch_dequant(const Launch& L, const CacheView& C, const int32_t* pt, int64
   const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
   if (C.fmt == K8V4_FORMAT_K8V4)
     dequant_kernel<K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, start, n_cells, k_out, v_rot_out, v_out, L.status);
+  else if (C.fmt == K8V4_FORMAT_Q4)
+    dequant_kernel<K8V4_FORMAT_Q4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, start, n_cells, k_out, v_rot_out, v_out, L.status);
   else
     dequant_kernel<K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, start, n_cells, k_out, v_rot_out, v_out, L.status);
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;

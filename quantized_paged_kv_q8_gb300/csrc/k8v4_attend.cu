@@ -1,8 +1,8 @@
-// Split-K flash-decode attention over the k8v4 (or INT8) paged cache: decode
-// (one query per sequence), the fused decode step (append the newest token, then
-// decode), and verify over the INT8 comparison format (n_q queries per sequence
-// with per-query step arrays; k8v4 verify runs in k8v4_prefill.cu or
-// k8v4_verify.cu).  The fused "mode 3" attention of the hybrid-KV pull request
+// Split-K flash-decode attention over the k8v4 (or INT8, or Q4) paged cache:
+// decode (one query per sequence), the fused decode step (append the newest
+// token, then decode), and verify over the INT8 and Q4 comparison formats (n_q
+// queries per sequence with per-query step arrays; k8v4 verify runs in
+// k8v4_prefill.cu or k8v4_verify.cu).  The fused "mode 3" attention of the hybrid-KV pull request
 // ("How": the K loader takes the int8 branch, the V loop the q4 branch, q is not
 // rotated and the output is rotated back; "Tests": step and batched forms with
 // per-query step arrays).
@@ -16,7 +16,10 @@
 //   QK^T: A = K codes (16 cells x 16 dims, int8 -> fp16 exactly), B = q (fp16,
 //         scaled per head by a power of two; an fp32 q is split into two fp16
 //         terms), separate fp32 accumulators for the two 128-lane halves so the
-//         two K scales apply after the MMA.
+//         two K scales apply after the MMA.  Q4 format (K rotated q4_0 like
+//         V): A = K nibbles (ldmatrix, nibble -> fp16 exactly), B = (H/16) q
+//         rotated once per warp in fp32 and split into two fp16 terms, a fresh
+//         accumulator per 32-lane block scaled by that block's d per cell.
 //   PV:   A = V codes (16 rotated dims x 16 cells, nibble -> bf16 exactly via
 //         ldmatrix.trans), B = p * d per 32-lane block, split into three bf16
 //         terms (24 significant bits), accumulated in fp32 in rotated space.
@@ -52,13 +55,21 @@ constexpr int kPlanes = K8V4_PV_PLANES;   // bf16 terms of p * d (3 = 24 signifi
 
 template <int FMT>
 struct Stage {
-  static constexpr int kK = 0;                                            // K codes [16][256], swizzled
-  static constexpr int kV = 16 * 256;                                     // V [16][128 or 256], swizzled
-  static constexpr int kVBytes = FMT == K8V4_FORMAT_K8V4 ? 16 * 128 : 16 * 256;
-  static constexpr int kKs = kV + kVBytes;                                // K scales [16][2] f32
-  static constexpr int kVs = kKs + 16 * 8;                                // V scales [16][8] f16 or [16][2] f32
-  static constexpr int kBytes = kVs + (FMT == K8V4_FORMAT_K8V4 ? 16 * 16 : 16 * 8);
+  static constexpr int kKBytes = FMT == K8V4_FORMAT_Q4 ? 16 * 128 : 16 * 256;    // int8 codes or nibbles
+  static constexpr int kVBytes = FMT == K8V4_FORMAT_INT8 ? 16 * 256 : 16 * 128;  // nibbles or int8 codes
+  static constexpr int kKsBytes = FMT == K8V4_FORMAT_Q4 ? 16 * 16 : 16 * 8;      // [16][8] f16 or [16][2] f32
+  static constexpr int kVsBytes = FMT == K8V4_FORMAT_INT8 ? 16 * 8 : 16 * 16;
+  static constexpr int kK = 0;                                            // K [16][256 or 128], swizzled
+  static constexpr int kV = kKBytes;                                      // V [16][128 or 256], swizzled
+  static constexpr int kKs = kV + kVBytes;
+  static constexpr int kVs = kKs + kKsBytes;
+  static constexpr int kBytes = kVs + kVsBytes;
 };
+__host__ __device__ constexpr int stage_bytes_of(int fmt) {
+  return fmt == K8V4_FORMAT_K8V4 ? Stage<K8V4_FORMAT_K8V4>::kBytes
+         : fmt == K8V4_FORMAT_Q4 ? Stage<K8V4_FORMAT_Q4>::kBytes
+                                 : Stage<K8V4_FORMAT_INT8>::kBytes;
+}
 
 struct AttendParams {
   CacheView C;
@@ -98,6 +109,11 @@ __device__ __forceinline__ void ldmatrix_x4_t(uint32_t r[4], uint32_t addr) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -129,6 +145,13 @@ __device__ __forceinline__ uint32_t nib_to_bf16(uint32_t r, int k) {
   __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t), bias);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// two nibbles at bits k and k+16 -> fp16x2 of (n - 8), exact: 0x64XX is 1024 + XX
+__device__ __forceinline__ uint32_t nib_to_f16(uint32_t r, int k) {
+  uint32_t t = ((r >> k) & 0x000f000fu) | 0x64006400u;
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  __half2 v = __hsub2(*reinterpret_cast<__half2*>(&t), bias);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 // bytes k0 and k1 of r (int8 codes) -> bf16x2 {c_k0, c_k1}, exact
 __device__ __forceinline__ uint32_t i8_to_bf16(uint32_t r, uint32_t s0, uint32_t s1) {
   const uint32_t u = r ^ 0x80808080u;
@@ -153,19 +176,30 @@ __device__ __forceinline__ void load_tile(const CacheView& C, uint32_t s, const 
                                           int tid, int nthr_rt) {
   const int nthr = NTHR > 0 ? NTHR : nthr_rt;
   const int H = C.H;
+  constexpr int kRow = FMT == K8V4_FORMAT_Q4 ? 128 : 256;                 // K bytes per (cell, head)
+  constexpr int vRow = FMT == K8V4_FORMAT_INT8 ? 256 : 128;
   const int64_t r0 = static_cast<int64_t>(slot0) * H + g;       // (cell, head) index of the tile's first row
-  const uint8_t* kb = base + r0 * 256;
-  const uint8_t* vb = base + C.v_off() + r0 * C.v_row_bytes();
-  const uint8_t* ksb = base + C.ks_off() + r0 * 8;
-  const uint8_t* vsb = base + C.vs_off() + r0 * C.vs_row_bytes();
-  const int kst = H * 256, vst = H * C.v_row_bytes();
-  // K codes: 16 cells x 16 chunks; chunk kk of cell j stored at kk ^ (4 * (j & 1))
+  const uint8_t* kb = base + r0 * kRow;
+  const uint8_t* vb = base + C.v_off() + r0 * vRow;
+  const uint8_t* ksb = base + C.ks_off() + r0 * (FMT == K8V4_FORMAT_Q4 ? 16 : 8);
+  const uint8_t* vsb = base + C.vs_off() + r0 * (FMT == K8V4_FORMAT_INT8 ? 8 : 16);
+  const int kst = H * kRow, vst = H * vRow;
+  if (FMT == K8V4_FORMAT_Q4) {
+    // K nibbles: 16 cells x 8 blocks; block b of cell j stored at b ^ (j & 7)
 #pragma unroll
-  for (int i = tid; i < 256; i += nthr) {
-    const int j = i >> 4, kk = i & 15;
-    cp_async16(s + Stage<FMT>::kK + j * 256 + 16 * (kk ^ ((j & 1) << 2)), kb + j * kst + 16 * kk);
+    for (int i = tid; i < 128; i += nthr) {
+      const int j = i >> 3, bb = i & 7;
+      cp_async16(s + Stage<FMT>::kK + j * 128 + 16 * (bb ^ (j & 7)), kb + j * kst + 16 * bb);
+    }
+  } else {
+    // K codes: 16 cells x 16 chunks; chunk kk of cell j stored at kk ^ (4 * (j & 1))
+#pragma unroll
+    for (int i = tid; i < 256; i += nthr) {
+      const int j = i >> 4, kk = i & 15;
+      cp_async16(s + Stage<FMT>::kK + j * 256 + 16 * (kk ^ ((j & 1) << 2)), kb + j * kst + 16 * kk);
+    }
   }
-  if (FMT == K8V4_FORMAT_K8V4) {
+  if (FMT != K8V4_FORMAT_INT8) {
     // V nibbles: 16 cells x 8 blocks; block b of cell j stored at b ^ (j & 7)
 #pragma unroll
     for (int i = tid; i < 128; i += nthr) {
@@ -183,8 +217,9 @@ __device__ __forceinline__ void load_tile(const CacheView& C, uint32_t s, const 
   for (int i = tid; i < 32; i += nthr) {
     const int j = i & 15;
     if (i < 16) {
-      cp_async8(s + Stage<FMT>::kKs + 8 * j, ksb + j * (H * 8));
-    } else if (FMT == K8V4_FORMAT_K8V4) {
+      if (FMT == K8V4_FORMAT_Q4) cp_async16(s + Stage<FMT>::kKs + 16 * j, ksb + j * (H * 16));
+      else cp_async8(s + Stage<FMT>::kKs + 8 * j, ksb + j * (H * 8));
+    } else if (FMT != K8V4_FORMAT_INT8) {
       cp_async16(s + Stage<FMT>::kVs + 16 * j, vsb + j * (H * 16));
     } else {
       cp_async8(s + Stage<FMT>::kVs + 8 * j, vsb + j * (H * 8));
@@ -201,7 +236,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
   asm volatile("griddepcontrol.wait;" ::: "memory");
   using S = Stage<FMT>;
   constexpr int kMT = 16;                                 // PV m-tiles (16 dims each)
-  constexpr int kBlocks = FMT == K8V4_FORMAT_K8V4 ? 8 : 2; // scale blocks per head
+  constexpr int kBlocks = FMT == K8V4_FORMAT_INT8 ? 2 : 8;  // V scale blocks per head
+  constexpr bool kQ4 = FMT == K8V4_FORMAT_Q4;
+  constexpr bool kLo = QF32 || kQ4;                         // q carried as two fp16 terms
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int qi = warp % p.n_q, gi = warp / p.n_q;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -239,11 +276,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
           uint8_t* base = C.pages + page * C.page_bytes;
           const int64_t r = static_cast<int64_t>(cell % C.P) * C.H + g;
           const int64_t elem = (static_cast<int64_t>(b) * C.H + g) * kD + 8 * lane;
+          // each warp's rotation scratch (the pipeline has not started)
+          long long* ts = reinterpret_cast<long long*>(smem) + warp * kRotScratch;
           if (warp == 0) {
-            if (p.kv_bf16) append_k_row<true>(C, base, r, p.k_new, elem, lane);
-            else append_k_row<false>(C, base, r, p.k_new, elem, lane);
+            if (p.kv_bf16) append_k_row<true, FMT>(C, base, r, p.k_new, elem, lane, ts);
+            else append_k_row<false, FMT>(C, base, r, p.k_new, elem, lane, ts);
           } else {
-            long long* ts = reinterpret_cast<long long*>(smem);   // the rotation's scratch (pipeline not started)
             if (p.kv_bf16) append_v_row<true, FMT>(C, base, r, p.v_new, elem, lane, ts);
             else append_v_row<false, FMT>(C, base, r, p.v_new, elem, lane, ts);
           }
@@ -255,34 +293,78 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     }
   }
 
-  // ---- q fragments (B operand of QK^T): lane holds head r0, dims 64i + 16c + 4j + e
+  // ---- q fragments (B operand of QK^T).  Int8 K: lane holds head r0, dims
+  // 64i + 16c + 4j + e (k-step 4i + j).  Q4 K: the rotated query (H/16) q, dims
+  // 32 blk + 16 hf + 4c + e (k-step 2 blk + hf) -- the dims of the nibble bytes
+  // 4c .. 4c+3 of block blk that ldmatrix hands this lane
   uint32_t qf[16][2];
-  uint32_t qf_lo[QF32 ? 16 : 1][2];
+  uint32_t qf_lo[kLo ? 16 : 1][2];
   float fscale;                                    // per head: sm_scale * log2(e) / 2^qexp
   {
     const int64_t qrow = ((static_cast<int64_t>(b) * p.n_q + qi) * HQ + g * kGqa + r0) * kD;
     float qv[64];
+    if (kQ4) {
+      // qv[8 blk + 4 hf + e] = q[32 blk + 16 hf + 4c + e]
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t e0 = qrow + 64 * i + 16 * c;
-      if (QF32) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + e0);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float4 v4 = src[t];
-          qv[16 * i + 4 * t] = v4.x; qv[16 * i + 4 * t + 1] = v4.y;
-          qv[16 * i + 4 * t + 2] = v4.z; qv[16 * i + 4 * t + 3] = v4.w;
+      for (int t4 = 0; t4 < 16; ++t4) {
+        const int64_t e0 = qrow + 16 * t4 + 4 * c;
+        if (QF32) {
+          const float4 v4 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + e0);
+          qv[4 * t4] = v4.x; qv[4 * t4 + 1] = v4.y; qv[4 * t4 + 2] = v4.z; qv[4 * t4 + 3] = v4.w;
+        } else {
+          const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + e0);
+          qv[4 * t4] = __uint_as_float(raw.x << 16);
+          qv[4 * t4 + 1] = __uint_as_float(raw.x & 0xffff0000u);
+          qv[4 * t4 + 2] = __uint_as_float(raw.y << 16);
+          qv[4 * t4 + 3] = __uint_as_float(raw.y & 0xffff0000u);
         }
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + e0);
+      }
+      // (H/16) q: a butterfly per index bit -- the six in-register bits of t
+      // (dims bits 0, 1, 4, 5, 6, 7), then lane bits 0 and 1 (dims bits 2, 3)
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint4 raw = src[t];
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int hb = 1; hb < 64; hb <<= 1) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            qv[16 * i + 8 * t + 2 * u] = __uint_as_float(w[u] << 16);
-            qv[16 * i + 8 * t + 2 * u + 1] = __uint_as_float(w[u] & 0xffff0000u);
+        for (int t = 0; t < 64; ++t) {
+          if (t & hb) continue;
+          const float x0 = qv[t], x1 = qv[t + hb];
+          qv[t] = x0 + x1;
+          qv[t + hb] = x0 - x1;
+        }
+      }
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+          const float o2 = __shfl_xor_sync(kFull, qv[t], m);
+          qv[t] = upper ? o2 - qv[t] : qv[t] + o2;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 64; ++t) qv[t] *= 0.0625f;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t e0 = qrow + 64 * i + 16 * c;
+        if (QF32) {
+          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + e0);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float4 v4 = src[t];
+            qv[16 * i + 4 * t] = v4.x; qv[16 * i + 4 * t + 1] = v4.y;
+            qv[16 * i + 4 * t + 2] = v4.z; qv[16 * i + 4 * t + 3] = v4.w;
+          }
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + e0);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint4 raw = src[t];
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              qv[16 * i + 8 * t + 2 * u] = __uint_as_float(w[u] << 16);
+              qv[16 * i + 8 * t + 2 * u + 1] = __uint_as_float(w[u] & 0xffff0000u);
+            }
           }
         }
       }
@@ -299,19 +381,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     fscale = p.sm_scale_log2 * ldexpf(1.0f, -sh);
 #pragma unroll
     for (int ks = 0; ks < 16; ++ks) {
-      const int o = 16 * (ks >> 2) + 4 * (ks & 3);
+      // b0 = (k 2c, 2c+1), b1 = (k 2c+8, 2c+9): int8 K dims o+0, o+1 | o+2, o+3;
+      // Q4 K (bytes 4c, 4c+2 | 4c+1, 4c+3 of the block) dims o+0, o+2 | o+1, o+3
+      const int o = kQ4 ? 4 * ks : 16 * (ks >> 2) + 4 * (ks & 3);
       float v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(qv[o + e], up);
+      for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(qv[o + (kQ4 ? ((e & 1) << 1) | (e >> 1) : e)], up);
       const __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
       qf[ks][0] = *reinterpret_cast<const uint32_t*>(&h0);
       qf[ks][1] = *reinterpret_cast<const uint32_t*>(&h1);
-      if (QF32) {
+      if (kLo) {
         const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
         const __half2 l0 = __floats2half2_rn(v[0] - f0.x, v[1] - f0.y);
         const __half2 l1 = __floats2half2_rn(v[2] - f1.x, v[3] - f1.y);
-        qf_lo[ks % (QF32 ? 16 : 1)][0] = *reinterpret_cast<const uint32_t*>(&l0);
-        qf_lo[ks % (QF32 ? 16 : 1)][1] = *reinterpret_cast<const uint32_t*>(&l1);
+        qf_lo[ks % (kLo ? 16 : 1)][0] = *reinterpret_cast<const uint32_t*>(&l0);
+        qf_lo[ks % (kLo ? 16 : 1)][1] = *reinterpret_cast<const uint32_t*>(&l1);
       }
     }
   }
@@ -384,51 +468,112 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     const uint8_t* st = gbuf + cur * S::kBytes;
     const uint32_t st_s = smem_u32(st);
 
-    // ---- QK^T: S^T[cell][head], halves accumulated separately; two
-    // accumulators per half keep four independent MMA chains in flight
-    float acc[4][4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 ka = lds128(st_s + S::kK + r0 * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
-      const uint4 kb = lds128(st_s + S::kK + (r0 + 8) * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
-      const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
-      uint32_t a[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        codes_to_f16(wa[j], a[j][0], a[j][2]);
-        codes_to_f16(wb[j], a[j][1], a[j][3]);
-      }
-#if K8V4_QF_SMEM
-      const uint4 qa = qsm[(2 * i) * 32 + lane], qb = qsm[(2 * i + 1) * 32 + lane];
-      const uint32_t qq[4][2] = {{qa.x, qa.y}, {qa.z, qa.w}, {qb.x, qb.y}, {qb.z, qb.w}};
-#endif
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float* dst = acc[2 * (i >> 1) + (j & 1)];
-#if K8V4_QF_SMEM
-        mma_f16(dst, a[j], qq[j][0], qq[j][1]);
-#else
-        mma_f16(dst, a[j], qf[4 * i + j][0], qf[4 * i + j][1]);
-#endif
-        if (QF32) mma_f16(dst, a[j], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][0], qf_lo[(4 * i + j) % (QF32 ? 16 : 1)][1]);
-      }
-    }
-    float a0[4], a1[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      a0[t] = acc[0][t] + acc[1][t];
-      a1[t] = acc[2][t] + acc[3][t];
-    }
-    const float2 kA = *reinterpret_cast<const float2*>(st + S::kKs + 8 * r0);
-    const float2 kB = *reinterpret_cast<const float2*>(st + S::kKs + 8 * (r0 + 8));
+    // ---- QK^T: S^T[cell][head]
     const bool vA = cell0 + r0 < lim, vB = cell0 + r0 + 8 < lim;
     float sc[4];
-    sc[0] = vA ? (kA.x * a0[0] + kA.y * a1[0]) * f0 : -INFINITY;
-    sc[1] = vA ? (kA.x * a0[1] + kA.y * a1[1]) * f1 : -INFINITY;
-    sc[2] = vB ? (kB.x * a0[2] + kB.y * a1[2]) * f0 : -INFINITY;
-    sc[3] = vB ? (kB.x * a0[3] + kB.y * a1[3]) * f1 : -INFINITY;
+    if (kQ4) {
+      // rotated K nibbles: per 32-lane block a fresh accumulator over its two
+      // k-steps (low nibbles: block dims 0-15, high: 16-31) and both q terms,
+      // then scaled by the cell's d of that block; the hi and lo q terms take
+      // separate accumulators so four MMA chains are in flight
+      const uint4 dA4 = lds128(st_s + S::kKs + 16 * r0), dB4 = lds128(st_s + S::kKs + 16 * (r0 + 8));
+      const uint32_t dAw[4] = {dA4.x, dA4.y, dA4.z, dA4.w}, dBw[4] = {dB4.x, dB4.y, dB4.z, dB4.w};
+      float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const int mi = lane >> 3, rr = lane & 7;
+      const int lcell = rr + 8 * (mi & 1);
+#pragma unroll
+      for (int bp = 0; bp < 8; bp += 2) {
+        uint32_t R[4];
+        ldmatrix_x4(R, st_s + S::kK + lcell * 128 + 16 * ((bp + (mi >> 1)) ^ (lcell & 7)));
+        uint32_t alo[2][4], ahi[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ra = R[2 * h], rb = R[2 * h + 1];   // cells r0, r0 + 8: bytes 4c .. 4c+3
+          alo[h][0] = nib_to_f16(ra, 0); alo[h][1] = nib_to_f16(rb, 0);
+          alo[h][2] = nib_to_f16(ra, 8); alo[h][3] = nib_to_f16(rb, 8);
+          ahi[h][0] = nib_to_f16(ra, 4); ahi[h][1] = nib_to_f16(rb, 4);
+          ahi[h][2] = nib_to_f16(ra, 12); ahi[h][3] = nib_to_f16(rb, 12);
+        }
+        float acc[2][2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) acc[h][u][0] = acc[h][u][1] = acc[h][u][2] = acc[h][u][3] = 0.0f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ks = 2 * (bp + h) + hf;
+            mma_f16(acc[h][0], hf ? ahi[h] : alo[h], qf[ks][0], qf[ks][1]);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ks = 2 * (bp + h) + hf;
+            mma_f16(acc[h][1], hf ? ahi[h] : alo[h], qf_lo[ks % (kLo ? 16 : 1)][0], qf_lo[ks % (kLo ? 16 : 1)][1]);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int blk = bp + h;
+          uint32_t wa = dAw[blk >> 1], wb = dBw[blk >> 1];
+          const float2 fa = __half22float2(*reinterpret_cast<__half2*>(&wa));
+          const float2 fb = __half22float2(*reinterpret_cast<__half2*>(&wb));
+          const float da = (blk & 1) ? fa.y : fa.x, db = (blk & 1) ? fb.y : fb.x;
+          s4[0] = fmaf(da, acc[h][0][0] + acc[h][1][0], s4[0]);
+          s4[1] = fmaf(da, acc[h][0][1] + acc[h][1][1], s4[1]);
+          s4[2] = fmaf(db, acc[h][0][2] + acc[h][1][2], s4[2]);
+          s4[3] = fmaf(db, acc[h][0][3] + acc[h][1][3], s4[3]);
+        }
+      }
+      sc[0] = vA ? s4[0] * f0 : -INFINITY;
+      sc[1] = vA ? s4[1] * f1 : -INFINITY;
+      sc[2] = vB ? s4[2] * f0 : -INFINITY;
+      sc[3] = vB ? s4[3] * f1 : -INFINITY;
+    } else {
+      // int8 K: the two 128-lane halves accumulated separately (two
+      // accumulators per half keep four independent MMA chains in flight)
+      float acc[4][4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 ka = lds128(st_s + S::kK + r0 * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
+        const uint4 kb = lds128(st_s + S::kK + (r0 + 8) * 256 + 16 * ((4 * i + c) ^ ((r0 & 1) << 2)));
+        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+        uint32_t a[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          codes_to_f16(wa[j], a[j][0], a[j][2]);
+          codes_to_f16(wb[j], a[j][1], a[j][3]);
+        }
+#if K8V4_QF_SMEM
+        const uint4 qa = qsm[(2 * i) * 32 + lane], qb = qsm[(2 * i + 1) * 32 + lane];
+        const uint32_t qq[4][2] = {{qa.x, qa.y}, {qa.z, qa.w}, {qb.x, qb.y}, {qb.z, qb.w}};
+#endif
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float* dst = acc[2 * (i >> 1) + (j & 1)];
+#if K8V4_QF_SMEM
+          mma_f16(dst, a[j], qq[j][0], qq[j][1]);
+#else
+          mma_f16(dst, a[j], qf[4 * i + j][0], qf[4 * i + j][1]);
+#endif
+          if (QF32) mma_f16(dst, a[j], qf_lo[(4 * i + j) % (kLo ? 16 : 1)][0], qf_lo[(4 * i + j) % (kLo ? 16 : 1)][1]);
+        }
+      }
+      float a0[4], a1[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        a0[t] = acc[0][t] + acc[1][t];
+        a1[t] = acc[2][t] + acc[3][t];
+      }
+      const float2 kA = *reinterpret_cast<const float2*>(st + S::kKs + 8 * r0);
+      const float2 kB = *reinterpret_cast<const float2*>(st + S::kKs + 8 * (r0 + 8));
+      sc[0] = vA ? (kA.x * a0[0] + kA.y * a1[0]) * f0 : -INFINITY;
+      sc[1] = vA ? (kA.x * a0[1] + kA.y * a1[1]) * f1 : -INFINITY;
+      sc[2] = vB ? (kB.x * a0[2] + kB.y * a1[2]) * f0 : -INFINITY;
+      sc[3] = vB ? (kB.x * a0[3] + kB.y * a1[3]) * f1 : -INFINITY;
+    }
 
     // ---- online softmax (heads 2c, 2c+1)
     float t0 = fmaxf(sc[0], sc[2]), t1 = fmaxf(sc[1], sc[3]);
@@ -474,7 +619,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     const float2 P01 = make_float2(P[0], P[1]), P23 = make_float2(P[2], P[3]);
 
     // ---- PV in rotated space
-    if (FMT == K8V4_FORMAT_K8V4) {
+    if (FMT != K8V4_FORMAT_INT8) {
       uint4 dv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) dv[t] = *reinterpret_cast<const uint4*>(st + S::kVs + 16 * pc[t]);
@@ -579,7 +724,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
 #pragma unroll
   for (int mt = 0; mt < kMT; ++mt) {
     int d0;
-    if (FMT == K8V4_FORMAT_K8V4) d0 = 32 * (mt >> 1) + 16 * (mt & 1) + 2 * r0;
+    if (FMT != K8V4_FORMAT_INT8) d0 = 32 * (mt >> 1) + 16 * (mt & 1) + 2 * r0;
     else d0 = 16 * mt + 2 * r0;
     *reinterpret_cast<float2*>(mine + (2 * c) * 256 + d0) = make_float2(o[mt][0], o[mt][2]);
     *reinterpret_cast<float2*>(mine + (2 * c + 1) * 256 + d0) = make_float2(o[mt][1], o[mt][3]);
@@ -615,7 +760,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
         L += src[2056 + h] * sc2;
       }
     }
-    if (FMT == K8V4_FORMAT_K8V4) {
+    if (FMT != K8V4_FORMAT_INT8) {
 #pragma unroll
       for (int hh = 1; hh < 8; hh <<= 1) {
 #pragma unroll
@@ -696,8 +841,7 @@ AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len,
   if (n_q > 1 && pl.n_groups > 15) pl.n_groups = 15;   // named barriers 1..15
   pl.warps = pl.n_groups * n_q;
   const int tiles = max(1, (max_seq_len + 15) / 16);
-  const int stage_bytes = pl.n_groups * kStages * (C.fmt == K8V4_FORMAT_K8V4 ? Stage<K8V4_FORMAT_K8V4>::kBytes
-                                                                               : Stage<K8V4_FORMAT_INT8>::kBytes);
+  const int stage_bytes = pl.n_groups * kStages * stage_bytes_of(C.fmt);
   const int ctas_per_sm = max(1, min(4, (200 * 1024) / max(stage_bytes, 1)));
   const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
   const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm;
@@ -746,6 +890,12 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
     // k8v4 with n_q > 1 left above; here n_q == 1
     return f32 ? launch_impl<K8V4_FORMAT_K8V4, true, true>(L, p, plan, out)
                : launch_impl<K8V4_FORMAT_K8V4, false, true>(L, p, plan, out);
+  }
+  if (C.fmt == K8V4_FORMAT_Q4) {
+    if (f32) return one ? launch_impl<K8V4_FORMAT_Q4, true, true>(L, p, plan, out)
+                        : launch_impl<K8V4_FORMAT_Q4, true, false>(L, p, plan, out);
+    return one ? launch_impl<K8V4_FORMAT_Q4, false, true>(L, p, plan, out)
+               : launch_impl<K8V4_FORMAT_Q4, false, false>(L, p, plan, out);
   }
   if (f32) return one ? launch_impl<K8V4_FORMAT_INT8, true, true>(L, p, plan, out)
                       : launch_impl<K8V4_FORMAT_INT8, true, false>(L, p, plan, out);

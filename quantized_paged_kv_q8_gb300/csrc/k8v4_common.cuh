@@ -16,13 +16,17 @@ constexpr int kD = 256;   // head_dim
 constexpr int kGqa = 8;   // query heads per KV head
 
 // Bytes per (cell, head) of each format.  K8V4: 256 K codes + 8 (two fp32
-// scales) + 128 V nibbles + 16 (eight fp16 scales) = 408; INT8: 256 + 8 + 256 + 8.
-__host__ __device__ constexpr int cell_head_bytes(int fmt) { return fmt == K8V4_FORMAT_K8V4 ? 408 : 528; }
+// scales) + 128 V nibbles + 16 (eight fp16 scales) = 408; INT8: 256 + 8 + 256 +
+// 8 = 528; Q4: 128 + 16 + 128 + 16 = 288.
+__host__ __device__ constexpr int cell_head_bytes(int fmt) {
+  return fmt == K8V4_FORMAT_K8V4 ? 408 : fmt == K8V4_FORMAT_Q4 ? 288 : 528;
+}
 
 // Device view of a cache.  Page p starts at pages + p * page_bytes; inside it
-// the runs are K codes [P][H][256], K scales [P][H][2] f32, V (nibbles
-// [P][H][8][16] or int8 codes [P][H][256]) and V scales ([P][H][8] f16 or
-// [P][H][2] f32).  r = slot * H + head indexes a (cell, head) inside a run.
+// the runs are K ([P][H][256] int8 codes, or [P][H][8][16] nibbles for Q4),
+// K scales ([P][H][2] f32, or [P][H][8] f16 for Q4), V ([P][H][8][16] nibbles,
+// or [P][H][256] int8 codes for INT8) and V scales ([P][H][8] f16, or [P][H][2]
+// f32 for INT8).  r = slot * H + head indexes a (cell, head) inside a run.
 struct CacheView {
   uint8_t* pages;
   int64_t n_pages;
@@ -31,11 +35,15 @@ struct CacheView {
   int H;
   int fmt;
 
-  __host__ __device__ int64_t ks_off() const { return 256ll * H * P; }
-  __host__ __device__ int64_t v_off() const { return 264ll * H * P; }
-  __host__ __device__ int64_t vs_off() const { return (fmt == K8V4_FORMAT_K8V4 ? 392ll : 520ll) * H * P; }
-  __host__ __device__ int v_row_bytes() const { return fmt == K8V4_FORMAT_K8V4 ? 128 : 256; }
-  __host__ __device__ int vs_row_bytes() const { return fmt == K8V4_FORMAT_K8V4 ? 16 : 8; }
+  __host__ __device__ int k_row_bytes() const { return fmt == K8V4_FORMAT_Q4 ? 128 : 256; }
+  __host__ __device__ int ks_row_bytes() const { return fmt == K8V4_FORMAT_Q4 ? 16 : 8; }
+  __host__ __device__ int v_row_bytes() const { return fmt == K8V4_FORMAT_INT8 ? 256 : 128; }
+  __host__ __device__ int vs_row_bytes() const { return fmt == K8V4_FORMAT_INT8 ? 8 : 16; }
+  __host__ __device__ int64_t ks_off() const { return static_cast<int64_t>(k_row_bytes()) * H * P; }
+  __host__ __device__ int64_t v_off() const { return static_cast<int64_t>(k_row_bytes() + ks_row_bytes()) * H * P; }
+  __host__ __device__ int64_t vs_off() const {
+    return static_cast<int64_t>(k_row_bytes() + ks_row_bytes() + v_row_bytes()) * H * P;
+  }
 };
 
 // ---------------------------------------------------------------- status word

@@ -1,6 +1,7 @@
 // Device helpers shared by the append kernel and the fused decode step: the
 // loads of a 256-element row, the exact rotation y = RN((H x) / 16), the int8
-// and q4_0 quantisers, and the per-warp append of one (token, head) row.  A
+// and q4_0 quantisers, and the per-warp append of one (token, head) row (K and
+// V of the k8v4, INT8 and Q4 formats).  A
 // row is held 8 elements per lane (element 8 * lane + r); each function works
 // on one warp.
 //
@@ -316,26 +317,32 @@ __device__ __forceinline__ void quant_q4_store(const float y[8], int lane, uint8
 }
 
 // ------------------------------------------------------------------ row appends
-// K row of (token, head) r: int8 codes + two fp32 scales
-template <bool BF16>
+// K row of (token, head) r: int8 codes + two fp32 scales, or, in the Q4 format,
+// rotated q4_0 like V; ts is this warp's kRotScratch int64 of shared scratch
+// for the rotation (Q4 only)
+template <bool BF16, int FMT>
 __device__ __forceinline__ void append_k_row(const CacheView& C, uint8_t* base, int64_t r, const void* k, int64_t elem,
-                                             int lane) {
+                                             int lane, long long* ts) {
   float x[8];
   load8<BF16>(k, elem, x);
+  if (FMT == K8V4_FORMAT_Q4) {
+    rotate_exact(x, lane, ts);
+    quant_q4_store(x, lane, base + r * 128, base + C.ks_off() + r * 16);
+    return;
+  }
   uint2 kc;
   const float s = quant_int8_half(x, kc);
   const float s_hi = __shfl_xor_sync(kQFull, s, 16);
   *reinterpret_cast<uint2*>(base + r * 256 + 8 * lane) = kc;
   if (lane == 0) *reinterpret_cast<float2*>(base + C.ks_off() + r * 8) = make_float2(s, s_hi);
 }
-// V row: rotated q4_0 (k8v4) or int8 (the INT8 comparison format); ts is this
-// warp's kRotScratch int64 of shared scratch for the rotation
+// V row: rotated q4_0 (k8v4 and Q4) or int8 (the INT8 comparison format)
 template <bool BF16, int FMT>
 __device__ __forceinline__ void append_v_row(const CacheView& C, uint8_t* base, int64_t r, const void* v, int64_t elem,
                                              int lane, long long* ts) {
   float x[8];
   load8<BF16>(v, elem, x);
-  if (FMT == K8V4_FORMAT_K8V4) {
+  if (FMT != K8V4_FORMAT_INT8) {
     rotate_exact(x, lane, ts);
     quant_q4_store(x, lane, base + C.v_off() + r * 128, base + C.vs_off() + r * 16);
   } else {

@@ -35,8 +35,10 @@ def test_every_declared_symbol_is_exported(L):
 def test_bytes_per_cell(L):
     assert k8.k8v4_bytes_per_cell(k8.FORMAT_K8V4, 2) == 816
     assert k8.k8v4_bytes_per_cell(k8.FORMAT_INT8, 2) == 1056
+    assert k8.k8v4_bytes_per_cell(k8.FORMAT_Q4, 2) == 576
     assert k8.k8v4_bytes_per_cell(k8.FORMAT_K8V4, 1) == 408
-    assert k8.k8v4_bytes_per_cell(2, 2) == 0
+    assert k8.k8v4_bytes_per_cell(0, 2) == 0
+    assert k8.k8v4_bytes_per_cell(4, 2) == 0
     assert k8.k8v4_bytes_per_cell(k8.FORMAT_K8V4, 0) == 0
 
 
@@ -52,7 +54,7 @@ FAKE = ctypes.c_void_p(0x20000)
 
 @pytest.mark.parametrize("bad,code", [
     (dict(head_dim=128), k8.EINVAL), (dict(page_size=8), k8.EINVAL), (dict(page_size=24), k8.EINVAL),
-    (dict(n_kv_heads=9), k8.EINVAL), (dict(format=2), k8.EINVAL), (dict(n_pages=0), k8.EINVAL),
+    (dict(n_kv_heads=9), k8.EINVAL), (dict(format=0), k8.EINVAL), (dict(format=4), k8.EINVAL), (dict(n_pages=0), k8.EINVAL),
     (dict(pages=0), k8.EINVAL), (dict(pages=0x10010), k8.EALIGN),
 ])
 def test_bad_cache_descriptor_rejected(L, bad, code):
@@ -75,6 +77,8 @@ def test_bad_arguments_rejected(L):
     assert L.attn_k8v4_prefill(d, FAKE, k8.F32, FAKE, 4, 64, 8, None, 0.0625, FAKE, None) == k8.EINVAL
     d8 = ctypes.byref(_desc(format=k8.FORMAT_INT8))
     assert L.attn_k8v4_prefill(d8, FAKE, k8.BF16, FAKE, 4, 64, 8, None, 0.0625, FAKE, None) == k8.EINVAL
+    d4 = ctypes.byref(_desc(format=k8.FORMAT_Q4))
+    assert L.attn_k8v4_prefill(d4, FAKE, k8.BF16, FAKE, 4, 64, 8, None, 0.0625, FAKE, None) == k8.EINVAL
     assert L.attn_k8v4_prefill(d, FAKE, k8.BF16, FAKE, 4, 64, 65, None, 0.0625, FAKE, None) == k8.EINVAL
     # dequant range
     assert L.kv_dequant_k8v4(d, FAKE, 4, 60, 5, FAKE, FAKE, None, None) == k8.EINVAL

@@ -37,9 +37,10 @@ def test_append_tiny_fp32_roundtrip_bytes():
             assert np.all(pages[p] == CANARY)
 
 
-def test_append_bf16_32k_bytes():
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_Q4])
+def test_append_bf16_32k_bytes(fmt):
     w = synth.config2()
-    gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv)
+    gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv, fmt)
     k = synth.Tensor(w.k.f32[None], "bf16")
     v = synth.Tensor(w.v.f32[None], "bf16")
     append_both(gpu, ref, w.page_table, w.pos, k, v)
@@ -48,10 +49,10 @@ def test_append_bf16_32k_bytes():
     _assert_bytes_equal(gpu, ref)
 
 
-@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8])
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8, k8.FORMAT_Q4])
 def test_append_shared_pool_chunks(fmt):
     """Three sequences in one interleaved pool, written in two appends (a history
-    then a chunk at its offset), ragged lengths, both formats."""
+    then a chunk at its offset), ragged lengths, every format."""
     seed = synth.config_seed(4) + 17
     lens = np.array([700, 1333, 64], np.int32)
     P = 64
@@ -71,9 +72,11 @@ def test_append_shared_pool_chunks(fmt):
     _assert_bytes_equal(gpu, ref)
 
 
-def test_append_exact_rotation_wide_exponents():
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_Q4])
+def test_append_exact_rotation_wide_exponents(fmt):
     """fp32 V rows whose values span far more than 2^55 (the rotation's slow path),
-    subnormals, all-zero rows, and rows with one huge value: bytes still equal."""
+    subnormals, all-zero rows, and rows with one huge value: bytes still equal
+    (in the Q4 format the K rows take the rotation too)."""
     rng = np.random.default_rng(123)
     n, P = 64, 16
     k = rng.standard_normal((1, n, 2, 256)).astype(np.float32)
@@ -87,18 +90,21 @@ def test_append_exact_rotation_wide_exponents():
     k[0, 5, 0, :128] = 0.0
     k[0, 6, 1, :] = (rng.standard_normal(256) * 1e-38).astype(np.float32)
     v[0, 7, 0, ::3] *= 2.0 ** 60
+    k[0, 8, 0, :] = (rng.standard_normal(256) * 10.0 ** rng.integers(-35, 35, 256)).astype(np.float32)
+    k[0, 9, 1, ::5] *= 2.0 ** 70
     pt = np.random.default_rng(5).permutation(n // P)[None].astype(np.int32)
-    gpu, ref = make_caches(n // P, P)
+    gpu, ref = make_caches(n // P, P, 2, fmt)
     append_both(gpu, ref, pt, np.array([0]), synth.Tensor(k, "f32"), synth.Tensor(v, "f32"))
     torch.cuda.synchronize()
     assert k8.k8v4_last_device_status() == 0
     _assert_bytes_equal(gpu, ref)
 
 
-@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8])
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8, k8.FORMAT_Q4])
 def test_dequant_matches_oracle(fmt):
-    """kv_dequant_k8v4: Khat = c*s, Vhat_rot = (q-8)*d and the exact inverse
-    rotation equal the oracle's dequantisation bit for bit."""
+    """kv_dequant_k8v4: Khat = c*s (Q4: the exact inverse rotation of the stored
+    K), Vhat_rot = (q-8)*d and the exact inverse rotation equal the oracle's
+    dequantisation bit for bit."""
     w = synth.config1()
     gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv, fmt)
     pt_d = append_both(gpu, ref, w.page_table, w.pos, synth.Tensor(w.k.f32[None], "f32"),

@@ -21,10 +21,11 @@ def _single_seq(w, fmt=k8.FORMAT_K8V4, dtype=None):
     return gpu, ref, pt_d
 
 
-def test_decode_tiny_fp32():
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_Q4])
+def test_decode_tiny_fp32(fmt):
     """Config 1: 1,024 fp32 cells with ties, one fp32 decode query."""
     w = synth.config1()
-    gpu, ref, pt_d = _single_seq(w)
+    gpu, ref, pt_d = _single_seq(w, fmt)
     got = decode_gpu(gpu, dev_tensor(w.q, (1, 16, 256)), pt_d, w.seq_lens, int(w.seq_lens[0]))
     rs, rh, rv = oracle.decode_rows(1, 16, w.seq_lens)
     want = ref.attention(w.page_table, rs, rh, rv, w.q.f32.reshape(-1, 256))
@@ -32,7 +33,7 @@ def test_decode_tiny_fp32():
     assert k8.k8v4_last_device_status() == 0
 
 
-@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8])
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8, k8.FORMAT_Q4])
 def test_decode_ragged_lengths(fmt):
     """One 5,000-cell cache read by 9 sequences that share its page table and see
     1, 15, 16, 17, 37, 1,000, 4,095, 4,999 and 5,000 cells (ragged tails, tiles
@@ -128,7 +129,7 @@ def test_verify_small(n_q):
     assert rel_err(got.reshape(-1, 256), want) <= TOL
 
 
-@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8])
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8, k8.FORMAT_Q4])
 @pytest.mark.parametrize("P,qdt", [(16, "f32"), (64, "bf16")])
 def test_verify_irregular_steps(fmt, P, qdt):
     """Verify with irregular per-query steps (0, 1, page and tile edges,
@@ -204,10 +205,10 @@ def test_verify_config4_full_sampled():
 @pytest.mark.parametrize("n_cells", [237568, 262144, 118784 + 37])
 def test_decode_long_context(n_cells):
     """Config 3 lengths (and one non-aligned length): all 16 rows against the oracle;
-    the INT8 comparison arm at the 238K point too."""
+    the INT8 and Q4 comparison arms at the 238K point too."""
     seed = synth.config_seed(3)
     w = synth.config3(n_cells, seed=seed)
-    fmts = [k8.FORMAT_K8V4] + ([k8.FORMAT_INT8] if n_cells == 237568 else [])
+    fmts = [k8.FORMAT_K8V4] + ([k8.FORMAT_INT8, k8.FORMAT_Q4] if n_cells == 237568 else [])
     for fmt in fmts:
         gpu, ref, pt_d = _single_seq(w, fmt)
         got = decode_gpu(gpu, dev_tensor(w.q, (1, 16, 256)), pt_d, w.seq_lens, n_cells)

@@ -41,7 +41,8 @@ def _setup(fmt, kvdt, lens, P=64, seed_off=0):
 
 @pytest.mark.parametrize("fmt,kvdt,P", [(k8.FORMAT_K8V4, "bf16", 64), (k8.FORMAT_K8V4, "f32", 64),
                                           (k8.FORMAT_INT8, "bf16", 64), (k8.FORMAT_INT8, "f32", 64),
-                                          (k8.FORMAT_K8V4, "bf16", 16), (k8.FORMAT_K8V4, "bf16", 256)])
+                                          (k8.FORMAT_K8V4, "bf16", 16), (k8.FORMAT_K8V4, "bf16", 256),
+                                          (k8.FORMAT_Q4, "bf16", 64), (k8.FORMAT_Q4, "f32", 16)])
 def test_decode_step_equals_append_then_decode(fmt, kvdt, P):
     lens = [1, 17, 64, 1000, 5000, 0, 4097]
     pt, lens, q, gpu_a, gpu_b, ref, k_new, v_new = _setup(fmt, kvdt, lens, P=P)

@@ -145,12 +145,25 @@ __device__ __forceinline__ uint32_t nib_to_bf16(uint32_t r, int k) {
   __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t), bias);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-// two nibbles at bits k and k+16 -> fp16x2 of (n - 8), exact: 0x64XX is 1024 + XX
-__device__ __forceinline__ uint32_t nib_to_f16(uint32_t r, int k) {
-  uint32_t t = ((r >> k) & 0x000f000fu) | 0x64006400u;
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-  __half2 v = __hsub2(*reinterpret_cast<__half2*>(&t), bias);
-  return *reinterpret_cast<uint32_t*>(&v);
+// one word of nibble bytes b0..b3 -> four fp16x2 of (n - 8), exact:
+//   lo0 = {b0 & 15, b2 & 15}, lo1 = {b1 & 15, b3 & 15}, hi0 = {b0 >> 4, b2 >> 4}, hi1 = {b1 >> 4, b3 >> 4}.
+// 0x640n is 1024 + n in fp16 and 0x64n0 is 1024 + 16 n; (1024 + 16 n) / 16 - 72
+// = n - 8 is exact, so one fused multiply-add finishes a high nibble
+__device__ __forceinline__ void nibs_to_f16(uint32_t r, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
+  const uint32_t r8 = r >> 8;
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+  const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2c00), __ushort_as_half(0x2c00));  // 1/16
+  const __half2 m72 = __halves2half2(__ushort_as_half(0xd480), __ushort_as_half(0xd480));      // -72
+  uint32_t t0 = (r & 0x000f000fu) | 0x64006400u, t1 = (r8 & 0x000f000fu) | 0x64006400u;
+  uint32_t t2 = (r & 0x00f000f0u) | 0x64006400u, t3 = (r8 & 0x00f000f0u) | 0x64006400u;
+  __half2 v0 = __hsub2(*reinterpret_cast<__half2*>(&t0), bias);
+  __half2 v1 = __hsub2(*reinterpret_cast<__half2*>(&t1), bias);
+  __half2 v2 = __hfma2(*reinterpret_cast<__half2*>(&t2), sixteenth, m72);
+  __half2 v3 = __hfma2(*reinterpret_cast<__half2*>(&t3), sixteenth, m72);
+  lo0 = *reinterpret_cast<uint32_t*>(&v0);
+  lo1 = *reinterpret_cast<uint32_t*>(&v1);
+  hi0 = *reinterpret_cast<uint32_t*>(&v2);
+  hi1 = *reinterpret_cast<uint32_t*>(&v3);
 }
 // bytes k0 and k1 of r (int8 codes) -> bf16x2 {c_k0, c_k1}, exact
 __device__ __forceinline__ uint32_t i8_to_bf16(uint32_t r, uint32_t s0, uint32_t s1) {
@@ -474,8 +487,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
     if (kQ4) {
       // rotated K nibbles: per 32-lane block a fresh accumulator over its two
       // k-steps (low nibbles: block dims 0-15, high: 16-31) and both q terms,
-      // then scaled by the cell's d of that block; the hi and lo q terms take
-      // separate accumulators so four MMA chains are in flight
+      // then scaled by the cell's d of that block
       const uint4 dA4 = lds128(st_s + S::kKs + 16 * r0), dB4 = lds128(st_s + S::kKs + 16 * (r0 + 8));
       const uint32_t dAw[4] = {dA4.x, dA4.y, dA4.z, dA4.w}, dBw[4] = {dB4.x, dB4.y, dB4.z, dB4.w};
       float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -487,29 +499,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
         ldmatrix_x4(R, st_s + S::kK + lcell * 128 + 16 * ((bp + (mi >> 1)) ^ (lcell & 7)));
         uint32_t alo[2][4], ahi[2][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t ra = R[2 * h], rb = R[2 * h + 1];   // cells r0, r0 + 8: bytes 4c .. 4c+3
-          alo[h][0] = nib_to_f16(ra, 0); alo[h][1] = nib_to_f16(rb, 0);
-          alo[h][2] = nib_to_f16(ra, 8); alo[h][3] = nib_to_f16(rb, 8);
-          ahi[h][0] = nib_to_f16(ra, 4); ahi[h][1] = nib_to_f16(rb, 4);
-          ahi[h][2] = nib_to_f16(ra, 12); ahi[h][3] = nib_to_f16(rb, 12);
+        for (int h = 0; h < 2; ++h) {   // R[2h], R[2h + 1]: cells r0, r0 + 8, bytes 4c .. 4c+3
+          nibs_to_f16(R[2 * h], alo[h][0], alo[h][2], ahi[h][0], ahi[h][2]);
+          nibs_to_f16(R[2 * h + 1], alo[h][1], alo[h][3], ahi[h][1], ahi[h][3]);
         }
-        float acc[2][2][4];
+        float acc[2][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int u = 0; u < 2; ++u) acc[h][u][0] = acc[h][u][1] = acc[h][u][2] = acc[h][u][3] = 0.0f;
+        for (int h = 0; h < 2; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int ks = 2 * (bp + h) + hf;
-            mma_f16(acc[h][0], hf ? ahi[h] : alo[h], qf[ks][0], qf[ks][1]);
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int ks = 2 * (bp + h) + hf;
-            mma_f16(acc[h][1], hf ? ahi[h] : alo[h], qf_lo[ks % (kLo ? 16 : 1)][0], qf_lo[ks % (kLo ? 16 : 1)][1]);
+            mma_f16(acc[h], hf ? ahi[h] : alo[h], qf[ks][0], qf[ks][1]);
+            mma_f16(acc[h], hf ? ahi[h] : alo[h], qf_lo[ks % (kLo ? 16 : 1)][0], qf_lo[ks % (kLo ? 16 : 1)][1]);
           }
         }
 #pragma unroll
@@ -519,10 +522,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
           const float2 fa = __half22float2(*reinterpret_cast<__half2*>(&wa));
           const float2 fb = __half22float2(*reinterpret_cast<__half2*>(&wb));
           const float da = (blk & 1) ? fa.y : fa.x, db = (blk & 1) ? fb.y : fb.x;
-          s4[0] = fmaf(da, acc[h][0][0] + acc[h][1][0], s4[0]);
-          s4[1] = fmaf(da, acc[h][0][1] + acc[h][1][1], s4[1]);
-          s4[2] = fmaf(db, acc[h][0][2] + acc[h][1][2], s4[2]);
-          s4[3] = fmaf(db, acc[h][0][3] + acc[h][1][3], s4[3]);
+          s4[0] = fmaf(da, acc[h][0], s4[0]);
+          s4[1] = fmaf(da, acc[h][1], s4[1]);
+          s4[2] = fmaf(db, acc[h][2], s4[2]);
+          s4[3] = fmaf(db, acc[h][3], s4[3]);
         }
       }
       sc[0] = vA ? s4[0] * f0 : -INFINITY;

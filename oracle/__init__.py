@@ -193,6 +193,43 @@ class Cache:
         return out
 
 
+def stream_resolve(page_table: np.ndarray, seq_lens, slot_of_page, n_resident: int, n_dev_pages: int, P: int,
+                   max_seq_len: int):
+    """Block lookups of one streamed attention call, from the streaming pull
+    request ("kv: --kv k8v4 streams with --kv-resident", "How" and "Tests"): every
+    page a sequence reads is looked up; a page resident in VRAM is read from its
+    slot, a miss is copied from the host copy into a VRAM staging slot.
+
+    Readings (the pages give the mechanism, not an order): lookups run in
+    (sequence, page index) order over the pages that hold a sequence's first
+    min(seq_lens[b], max_seq_len) cells; the r-th miss takes staging slot
+    n_resident + r; a miss with no staging slot left (n_resident + r >=
+    n_dev_pages) is not read (-1) and reported; table entries no cell reaches are
+    -1.  Returns (device page table, [(host page, slot)] copies, overflow)."""
+    page_table = np.asarray(page_table)
+    n_seqs, max_pages = page_table.shape
+    dev = np.full((n_seqs, max_pages), -1, np.int32)
+    moves = []
+    rank = 0
+    overflow = False
+    for b in range(n_seqs):
+        n = min(max(int(seq_lens[b]), 0), max_seq_len)
+        for i in range((n + P - 1) // P):
+            hp = int(page_table[b, i])
+            s = int(slot_of_page[hp])
+            if s >= 0:
+                dev[b, i] = s
+                continue
+            slot = n_resident + rank
+            rank += 1
+            if slot < n_dev_pages:
+                dev[b, i] = slot
+                moves.append((hp, slot))
+            else:
+                overflow = True
+    return dev, moves, overflow
+
+
 def decode_rows(n_seqs: int, n_q_heads: int, seq_lens) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """Row descriptors for decode: row (b, h) sees seq_lens[b] cells."""
     b = np.repeat(np.arange(n_seqs), n_q_heads)

@@ -533,3 +533,78 @@ def test_q4_format_dequant_and_attention(orc):
             V = torch.tensor(vd[:vis, g])[None, None]
             ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=1.0 / 16.0)[0, 0, 0].numpy()
             assert np.max(np.abs(got[h] - ref)) < 1e-11 * max(1.0, np.max(np.abs(ref)))
+
+
+# ---------------------------------------------------------------- streaming block lookups
+def test_stream_resolve_worked_example(orc):
+    """A lookup worked by hand: P = 4, lengths 9 and 4 (three and one pages), host
+    pages 5, 2, 7 | 2; pages 2 and 7 resident in slots 0 and 1, two staging slots.
+    The one miss (page 5) goes to the first staging slot; page 2 is a hit for both
+    sequences; entries no cell reaches stay -1."""
+    pt = np.array([[5, 2, 7], [2, 0, 0]], np.int32)
+    slot_of_page = np.full(8, -1, np.int32)
+    slot_of_page[2], slot_of_page[7] = 0, 1
+    dev, moves, over = orc.stream_resolve(pt, [9, 4], slot_of_page, 2, 4, 4, 12)
+    assert dev.tolist() == [[2, 0, 1], [0, -1, -1]]
+    assert moves == [(5, 2)]
+    assert not over
+
+
+def test_stream_resolve_extremes_and_overflow(orc):
+    """Everything resident: the table is slot_of_page of the host table and
+    nothing moves.  Nothing resident: every needed page moves, in lookup order,
+    to consecutive staging slots.  One staging slot short: the last miss is not
+    read and overflow is reported.  Lengths are clipped to max_seq_len."""
+    rng = np.random.default_rng(3)
+    P, n_host = 16, 40
+    pt = rng.permutation(n_host)[:30].reshape(3, 10).astype(np.int32)
+    lens = [160, 17, 0]
+    need = [10, 2, 0]
+    every = rng.permutation(n_host).astype(np.int32)
+    dev, moves, over = orc.stream_resolve(pt, lens, every, n_host, n_host, P, 160)
+    for b in range(3):
+        assert dev[b, :need[b]].tolist() == [int(every[p]) for p in pt[b, :need[b]]]
+        assert np.all(dev[b, need[b]:] == -1)
+    assert moves == [] and not over
+    none = np.full(n_host, -1, np.int32)
+    dev, moves, over = orc.stream_resolve(pt, lens, none, 5, 5 + 12, P, 160)
+    order = [int(p) for b in range(3) for p in pt[b, :need[b]]]
+    assert moves == [(p, 5 + r) for r, p in enumerate(order)] and not over
+    assert dev[0, :10].tolist() == list(range(5, 15)) and dev[1, :2].tolist() == [15, 16]
+    dev, moves, over = orc.stream_resolve(pt, lens, none, 5, 5 + 11, P, 160)
+    assert over and len(moves) == 11 and dev[1, 1] == -1
+    dev, moves, over = orc.stream_resolve(pt, [1000, 17, 0], none, 0, 64, P, 48)
+    assert dev[0, :3].tolist() == [0, 1, 2] and np.all(dev[0, 3:] == -1)
+
+
+def test_stream_resolve_reads_the_right_bytes(orc):
+    """Invariant on random tables: emulate VRAM (resident slots filled from the
+    host copy, then the returned copies applied) and check that every cell a
+    sequence reads through the returned table holds the bytes of the host page
+    its own page table names, and that no copy overwrites a resident slot."""
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        P = int(rng.choice([16, 64]))
+        n_host, n_res = 50, int(rng.integers(0, 20))
+        n_seqs, max_pages = int(rng.integers(1, 5)), 8
+        pt = rng.integers(0, n_host, (n_seqs, max_pages)).astype(np.int32)
+        lens = rng.integers(0, max_pages * P + 1, n_seqs)
+        host = rng.integers(0, 256, (n_host, 4), dtype=np.uint8)
+        slot_of_page = np.full(n_host, -1, np.int32)
+        res_pages = rng.permutation(n_host)[:n_res]
+        slot_of_page[res_pages] = rng.permutation(n_res)
+        n_dev = n_res + n_seqs * max_pages
+        dev_mem = np.zeros((n_dev, 4), np.uint8)
+        for p in res_pages:
+            dev_mem[slot_of_page[p]] = host[p]
+        dev, moves, over = orc.stream_resolve(pt, lens, slot_of_page, n_res, n_dev, P, max_pages * P)
+        assert not over
+        for hp, slot in moves:
+            assert slot >= n_res
+            dev_mem[slot] = host[hp]
+        for b in range(n_seqs):
+            for i in range(max_pages):
+                if i * P < lens[b]:
+                    assert np.array_equal(dev_mem[dev[b, i]], host[pt[b, i]])
+                else:
+                    assert dev[b, i] == -1

@@ -288,6 +288,87 @@ def measure_batched_step(args, dev, n_seqs: int = 32, n_cells: int = 8192, reps:
             "gbs": CELL_BYTES * cells / (ms / 1e3) / 1e9, "cells_per_s": cells / (ms / 1e3)}
 
 
+def measure_stream(args, dev, resident_cells: int = 32768, reps: int = 20):
+    """KV streaming at the 238K workload: the page-locked host mirror holds all
+    3,712 pages, the device holds a resident window of the newest
+    `resident_cells` cells (512 pages, the streaming PR's --kv-resident 32768)
+    plus staging slots.  One streamed decode = kv_stream_resolve (the lookups and
+    the copy of every non-resident page from the mirror over NVLink-C2C) +
+    attn_k8v4_decode over the device table.  Also timed: the mirrored append of
+    the whole cache (both copies written), and a plain pinned host -> device
+    cudaMemcpyAsync of 256 MiB, the copy rate the page mover is compared with."""
+    import torch
+    import quantized_paged_kv_q8_gb300 as k8
+    import synth
+    w = synth.config3(N_CELLS)
+    need = N_CELLS // P
+    n_res = resident_cells // P
+    host = k8.PagedCache(w.n_pages, P, H, device="pinned")
+    devc = k8.PagedCache(n_res + need, P, H, device=dev)
+    slot_of_page = np.full(w.n_pages, -1, np.int32)
+    slot_of_page[w.page_table[0, need - n_res:need]] = np.arange(n_res, dtype=np.int32)
+    sop = torch.from_numpy(slot_of_page).to(dev)
+    pt = torch.from_numpy(w.page_table).to(dev)
+    kd = torch.from_numpy(w.k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, N_CELLS, H, 256).to(dev)
+    vd = torch.from_numpy(w.v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, N_CELLS, H, 256).to(dev)
+    zero = torch.zeros(1, dtype=torch.int64, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    k8.kv_append_k8v4_mirrored(host, devc, sop, pt, zero, kd, vd)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for _ in range(3):
+        k8.kv_append_k8v4_mirrored(host, devc, sop, pt, zero, kd, vd)
+    ev[1].record()
+    torch.cuda.synchronize()
+    append_ms = ev[0].elapsed_time(ev[1]) / 3
+    del kd, vd
+    q = torch.from_numpy(w.q.dev.view(np.int16)).view(torch.bfloat16).reshape(1, HQ, 256).to(dev)
+    lens = torch.full((1,), N_CELLS, dtype=torch.int32, device=dev)
+    dev_pt = torch.empty_like(pt)
+    sws = torch.empty(k8.kv_stream_workspace_bytes(1, pt.shape[1]), dtype=torch.uint8, device=dev)
+    out = torch.empty(1, HQ, 256, dtype=torch.float32, device=dev)
+    wsp = k8.workspace(devc, 1, 1, N_CELLS, device=dev)
+
+    def step():
+        k8.kv_stream_resolve(host, devc, sop, n_res, pt, lens, N_CELLS, dev_pt, sws)
+        k8.attn_k8v4_decode(devc, q, dev_pt, lens, N_CELLS, out, wsp)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ev[2].record()
+    for _ in range(reps):
+        step()
+    ev[3].record()
+    torch.cuda.synchronize()
+    step_ms = ev[2].elapsed_time(ev[3]) / reps
+    ev[2].record()
+    for _ in range(reps):
+        k8.kv_stream_resolve(host, devc, sop, n_res, pt, lens, N_CELLS, dev_pt, sws)
+    ev[3].record()
+    torch.cuda.synchronize()
+    resolve_ms = ev[2].elapsed_time(ev[3]) / reps
+    assert k8.k8v4_last_device_status() == 0
+    moved = (need - n_res) * devc.page_bytes
+    # the plain copy the mover is compared with: 256 MiB pinned -> device
+    src = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    ev[4].record()
+    for _ in range(5):
+        dst.copy_(src, non_blocking=True)
+    ev[5].record()
+    torch.cuda.synchronize()
+    h2d_gbs = 5 * (256 << 20) / (ev[4].elapsed_time(ev[5]) / 1e3) / 1e9
+    return {"workload": f"stream_decode_{N_CELLS}_cells_{resident_cells}_resident",
+            "resident_pages": n_res, "streamed_pages": need - n_res, "page_bytes": devc.page_bytes,
+            "ms_per_step": step_ms, "cells_per_s": N_CELLS / (step_ms / 1e3),
+            "resolve_copy_ms": resolve_ms, "copy_gbs": moved / (resolve_ms / 1e3) / 1e9,
+            "h2d_memcpy_gbs": h2d_gbs, "copy_frac_of_memcpy": moved / (resolve_ms / 1e3) / 1e9 / h2d_gbs,
+            "mirrored_append_ms": append_ms, "mirrored_append_cells_per_s": N_CELLS / (append_ms / 1e3)}
+
+
 def measure_prefill(args, dev, chunk: int, reps: int = 3):
     """Config 5: 229,376-cell history, then an append of `chunk` tokens at offset
     229,376 (timed: chunk append cells/s) and causal prefill of the chunk (timed:
@@ -345,7 +426,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="k8v4", choices=["k8v4", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify", "batched"],
+    ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify", "batched", "stream"],
                     help="lean single-kernel run for ncu (no replicas, INT8 arm, e2e or CPU baseline)")
     ap.add_argument("--chunk", type=int, default=8192, help="prefill chunk length (tokens)")
     args = ap.parse_args()
@@ -368,9 +449,10 @@ def main():
     buildlib.build()
     assert k8.k8v4_device_check() == 0, "libk8v4 needs an sm_103 device"
 
-    if args.profile in ("prefill", "verify", "batched"):
+    if args.profile in ("prefill", "verify", "batched", "stream"):
         res = (measure_prefill(args, dev, args.chunk) if args.profile == "prefill"
-               else measure_verify(args, dev) if args.profile == "verify" else measure_batched_step(args, dev))
+               else measure_verify(args, dev) if args.profile == "verify"
+               else measure_stream(args, dev) if args.profile == "stream" else measure_batched_step(args, dev))
         if rank == 0:
             print(json.dumps({"profile": args.profile, **res}), flush=True)
         return
@@ -512,6 +594,7 @@ def main():
     torch.cuda.empty_cache()
     verify = measure_verify(args, dev)
     batched = measure_batched_step(args, dev)
+    stream = measure_stream(args, dev)
     prefill = measure_prefill(args, dev, 8192)
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
@@ -542,6 +625,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "verify": {**verify, "frac_hbm": verify["gbs"] / hbm},
         "batched_step": {**batched, "frac_hbm": batched["gbs"] / hbm},
+        "stream": stream,
         "prefill": {**prefill, "frac_bf16_burst": prefill["tflops"] / bf16,
                     "frac_bf16_sustained": prefill["tflops"] / bf16_sus,
                     "peak_note": "bf16 dense cuBLAS peaks from MEASURED_PEAKS.json (burst and sustained); the "

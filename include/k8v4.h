@@ -220,6 +220,63 @@ int attn_k8v4_prefill(const k8v4_cache* cache, const void* q, int32_t q_dtype, c
 int kv_dequant_k8v4(const k8v4_cache* cache, const int32_t* page_table, int64_t max_pages, int64_t start,
                     int64_t n_cells, float* k_out, float* v_rot_out, float* v_out, void* stream);
 
+/* ---------------------------------------------------------------- streaming
+ * A streamed cache (the streaming PR, "How"): the authoritative copy of every
+ * page lives in a host mirror -- a k8v4_cache whose `pages` is page-locked host
+ * memory the device can address (cudaHostAlloc, or cudaHostRegister'ed), with
+ * the format, P and H of the device cache.  The device cache holds n_resident
+ * resident slots (slots 0 .. n_resident - 1) followed by staging slots that a
+ * streamed call fills with the pages it misses.  Every writer writes both
+ * copies (kv_append_k8v4_mirrored), so a page read from its resident slot and
+ * the same page copied from the mirror hold the same bytes, and attention over
+ * either is bitwise the same (the PR's "Tests").
+ *   slot_of_page: int32 [host n_pages] (device): the resident slot holding host
+ *                 page p (0 .. n_resident - 1), or -1 when p is not resident.
+ * A host pointer that is not page-locked memory mapped for the current device
+ * is rejected with K8V4_EINVAL before any launch. */
+
+/* Append to a streamed cache: page_table holds HOST page ids; every cell is
+ * written to its mirror page and, when slot_of_page[page] >= 0, to that device
+ * slot as well, from one quantisation (the PR's writers write both halves'
+ * host copies, "How").  Other arguments as kv_append_k8v4.  A slot value other
+ * than -1 outside [0, dev n_pages) is recorded (K8V4_ERANGE); the mirror is
+ * still written. */
+int kv_append_k8v4_mirrored(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* slot_of_page,
+                            const int32_t* page_table, int64_t max_pages, int32_t n_seqs, const int64_t* pos,
+                            int32_t n_tok, const void* k, const void* v, int32_t dtype, void* stream);
+
+/* Workspace bytes of kv_stream_resolve: 16 + 8 * n_seqs * max_pages (the copy
+ * list); 0 if n_seqs * max_pages exceeds 2^28. */
+size_t kv_stream_workspace_bytes(int32_t n_seqs, int64_t max_pages);
+
+/* The page lookups of one streamed attention call, and the copies of its misses
+ * (the PR's block resolve and copy, "How").  Every page that sequence b reads
+ * -- page indices below ceil(min(seq_lens[b], max_seq_len) / P) -- is looked
+ * up in (sequence, page index) order: a resident page maps to its slot; the
+ * r-th miss is copied from the mirror into staging slot n_resident + r.
+ *   page_table:     int32 [n_seqs][max_pages], host page ids (device memory).
+ *   seq_lens:       int32 [n_seqs] (device), the cells each sequence reads
+ *                   (decode: its length; verify: its largest step).
+ *   dev_page_table: int32 [n_seqs][max_pages] (device, written): the slot of
+ *                   every page read, -1 for entries no cell reaches.
+ *   workspace:      >= kv_stream_workspace_bytes(n_seqs, max_pages) bytes,
+ *                   16-byte aligned.
+ * Then attn_k8v4_decode / attn_k8v4_verify on the device cache with
+ * dev_page_table read exactly the bytes of the host pages.  Device-side: a miss
+ * with no staging slot left is not copied, its entry is -1 and K8V4_ENOSPACE is
+ * recorded; a host page id or slot value out of range gives -1 and
+ * K8V4_ERANGE.  A page two sequences share is copied once per miss. */
+int kv_stream_resolve(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* slot_of_page,
+                      int32_t n_resident, const int32_t* page_table, int64_t max_pages, const int32_t* seq_lens,
+                      int32_t n_seqs, int32_t max_seq_len, int32_t* dev_page_table, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Copy whole pages from the host mirror into device slots (all runs of a page):
+ * host page pages[i][0] -> slot pages[i][1] for i < n (e.g. to fill the
+ * resident window).  pages: int32 [n][2] (device), 8-byte aligned.  An id out of
+ * range is recorded (K8V4_ERANGE) and its copy skipped. */
+int kv_stream_copy(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* pages, int32_t n, void* stream);
+
 /* Synchronise `stream`, return the first device-side error recorded since the
  * last call (K8V4_OK if none) and clear it.  The word is per device and shared
  * by all streams. */

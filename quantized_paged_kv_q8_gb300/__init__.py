@@ -65,6 +65,10 @@ def lib():
             "attn_k8v4_prefill": ([C, P, I32, P, I64, I32, I32, P, F, P, P], ctypes.c_int),
             "kv_dequant_k8v4": ([C, P, I64, I64, I64, P, P, P, P], ctypes.c_int),
             "k8v4_last_device_status": ([P], ctypes.c_int),
+            "kv_append_k8v4_mirrored": ([C, C, P, P, I64, I32, P, I32, P, P, I32, P], ctypes.c_int),
+            "kv_stream_workspace_bytes": ([I32, I64], SZ),
+            "kv_stream_resolve": ([C, C, P, I32, P, I64, P, I32, I32, P, P, SZ, P], ctypes.c_int),
+            "kv_stream_copy": ([C, C, P, I32, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -78,7 +82,8 @@ EXPORTED = ("k8v4_bytes_per_cell", "k8v4_status_string", "k8v4_device_check", "k
             "attn_k8v4_workspace_bytes", "attn_k8v4_decode", "attn_k8v4_decode_noalloc", "attn_k8v4_decode_step",
             "attn_k8v4_verify",
             "attn_k8v4_prefill",
-            "kv_dequant_k8v4", "k8v4_last_device_status")
+            "kv_dequant_k8v4", "k8v4_last_device_status",
+            "kv_append_k8v4_mirrored", "kv_stream_workspace_bytes", "kv_stream_resolve", "kv_stream_copy")
 
 
 def status_string(code: int) -> str:
@@ -125,11 +130,16 @@ class PagedCache:
 
     def __init__(self, n_pages: int, page_size: int, n_kv_heads: int = 2, fmt: int = FORMAT_K8V4,
                  device: str | torch.device = "cuda", pages: torch.Tensor | None = None):
+        """device="pinned" allocates the pages in page-locked host memory: the
+        host mirror of a streamed cache."""
         self.n_pages, self.page_size, self.n_kv_heads, self.fmt = n_pages, page_size, n_kv_heads, fmt
         self.bytes_per_cell = k8v4_bytes_per_cell(fmt, n_kv_heads)
         self.page_bytes = page_size * self.bytes_per_cell
         nbytes = n_pages * self.page_bytes
-        if pages is None:
+        if pages is None and device == "pinned":
+            pages = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+            pages.zero_()
+        elif pages is None:
             pages = torch.zeros(nbytes, dtype=torch.uint8, device=device)
         assert pages.dtype == torch.uint8 and pages.numel() == nbytes and pages.is_contiguous()
         self.pages = pages
@@ -214,6 +224,43 @@ def kv_dequant_k8v4(cache: PagedCache, page_table: torch.Tensor, start: int, n_c
     rc = lib().kv_dequant_k8v4(cache.ref(), _ptr(page_table), page_table.shape[-1], start, n_cells, _ptr(k_out),
                                _ptr(v_rot_out), _ptr(v_out), _stream(stream))
     _check(rc, "kv_dequant_k8v4")
+
+
+def kv_append_k8v4_mirrored(host: PagedCache, dev: PagedCache, slot_of_page: torch.Tensor, page_table: torch.Tensor,
+                            pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    """Append to a streamed cache: page_table holds host page ids; every row goes to
+    the pinned mirror `host` and, where slot_of_page[page] >= 0, to that slot of `dev`."""
+    n_seqs, n_tok = k.shape[0], k.shape[1]
+    assert k.shape == v.shape and k.dtype == v.dtype and k.is_contiguous() and v.is_contiguous()
+    assert page_table.dtype == torch.int32 and pos.dtype == torch.int64 and slot_of_page.dtype == torch.int32
+    rc = lib().kv_append_k8v4_mirrored(host.ref(), dev.ref(), _ptr(slot_of_page), _ptr(page_table),
+                                       page_table.shape[-1], n_seqs, _ptr(pos), n_tok, _ptr(k), _ptr(v), _dtype(k),
+                                       _stream(stream))
+    _check(rc, "kv_append_k8v4_mirrored")
+
+
+def kv_stream_workspace_bytes(n_seqs: int, max_pages: int) -> int:
+    return int(lib().kv_stream_workspace_bytes(n_seqs, max_pages))
+
+
+def kv_stream_resolve(host: PagedCache, dev: PagedCache, slot_of_page: torch.Tensor, n_resident: int,
+                      page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                      dev_page_table: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """Look up the pages each sequence reads (resident slot, or a copy from the
+    mirror into a staging slot) and write the device page table."""
+    assert page_table.dtype == torch.int32 and dev_page_table.shape == page_table.shape
+    rc = lib().kv_stream_resolve(host.ref(), dev.ref(), _ptr(slot_of_page), n_resident, _ptr(page_table),
+                                 page_table.shape[-1], _ptr(seq_lens), page_table.shape[0], max_seq_len,
+                                 _ptr(dev_page_table), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "kv_stream_resolve")
+    return dev_page_table
+
+
+def kv_stream_copy(host: PagedCache, dev: PagedCache, pages: torch.Tensor, stream=None) -> None:
+    """Copy host pages pages[i, 0] into device slots pages[i, 1]."""
+    assert pages.dtype == torch.int32 and pages.is_contiguous() and pages.shape[-1] == 2
+    rc = lib().kv_stream_copy(host.ref(), dev.ref(), _ptr(pages), pages.shape[0], _stream(stream))
+    _check(rc, "kv_stream_copy")
 
 
 def k8v4_last_device_status(stream=None) -> int:

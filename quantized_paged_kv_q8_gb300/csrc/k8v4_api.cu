@@ -89,6 +89,26 @@ int check_table(const CacheView& v, const int32_t* pt, int64_t max_pages) {
   return K8V4_OK;
 }
 
+// The host mirror of a streamed cache: the same format, P and H as the device
+// cache, pages in page-locked host memory that the device can address.  Called
+// after make_launch (needs the device context); `M` gets the device-side address.
+int mirror_of(const k8v4_cache* host, const CacheView& C, CacheView* M) {
+  int rc = view_of(host, M);
+  if (rc) return rc;
+  if (M->fmt != C.fmt || M->P != C.P || M->H != C.H) return K8V4_EINVAL;
+  return K8V4_OK;
+}
+int mirror_address(const k8v4_cache* host, CacheView* M) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host->pages) != cudaSuccess) {
+    cudaGetLastError();                   // clear the error state the failed query left
+    return K8V4_EINVAL;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return K8V4_EINVAL;
+  M->pages = static_cast<uint8_t*>(a.devicePointer);
+  return K8V4_OK;
+}
+
 }  // namespace
 }  // namespace k8v4
 
@@ -227,6 +247,69 @@ int kv_dequant_k8v4(const k8v4_cache* cache, const int32_t* page_table, int64_t 
   Launch L;
   if ((rc = make_launch(stream, &L))) return rc;
   return launch_dequant(L, C, page_table, max_pages, start, n_cells, k_out, v_rot_out, v_out);
+}
+
+int kv_append_k8v4_mirrored(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* slot_of_page,
+                            const int32_t* page_table, int64_t max_pages, int32_t n_seqs, const int64_t* pos,
+                            int32_t n_tok, const void* k, const void* v, int32_t dtype, void* stream) {
+  CacheView C, M;
+  int rc = view_of(dev, &C);
+  if (rc) return rc;
+  if ((rc = mirror_of(host, C, &M))) return rc;
+  if ((rc = check_table(M, page_table, max_pages))) return rc;
+  if (n_seqs < 0 || n_tok < 0 || (dtype != K8V4_F32 && dtype != K8V4_BF16)) return K8V4_EINVAL;
+  if (n_seqs == 0 || n_tok == 0) return K8V4_OK;
+  if (!pos || !k || !v || !slot_of_page) return K8V4_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(pos, 8) || !aligned(slot_of_page, 4)) return K8V4_EALIGN;
+  Launch L;
+  if ((rc = make_launch(stream, &L))) return rc;
+  if ((rc = mirror_address(host, &M))) return rc;
+  return launch_append(L, C, page_table, max_pages, n_seqs, pos, n_tok, k, v, dtype, &M, slot_of_page);
+}
+
+size_t kv_stream_workspace_bytes(int32_t n_seqs, int64_t max_pages) {
+  if (n_seqs < 0 || max_pages < 1 || static_cast<int64_t>(n_seqs) * max_pages > (int64_t(1) << 28)) return 0;
+  return stream_ws_bytes(n_seqs, max_pages);
+}
+
+int kv_stream_resolve(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* slot_of_page, int32_t n_resident,
+                      const int32_t* page_table, int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs,
+                      int32_t max_seq_len, int32_t* dev_page_table, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  CacheView C, M;
+  int rc = view_of(dev, &C);
+  if (rc) return rc;
+  if ((rc = mirror_of(host, C, &M))) return rc;
+  if ((rc = check_table(M, page_table, max_pages))) return rc;
+  if (n_seqs < 0 || n_seqs > 65535 || static_cast<int64_t>(n_seqs) * max_pages > (int64_t(1) << 28))
+    return K8V4_EINVAL;
+  if (n_resident < 0 || n_resident > C.n_pages) return K8V4_EINVAL;
+  if (max_seq_len < 0 || static_cast<int64_t>(max_seq_len) > max_pages * C.P) return K8V4_EINVAL;
+  if (n_seqs == 0) return K8V4_OK;
+  if (!slot_of_page || !seq_lens || !dev_page_table || !workspace) return K8V4_EINVAL;
+  if (!aligned(slot_of_page, 4) || !aligned(seq_lens, 4) || !aligned(dev_page_table, 4) || !aligned(workspace, 16))
+    return K8V4_EALIGN;
+  if (workspace_bytes < stream_ws_bytes(n_seqs, max_pages)) return K8V4_ENOSPACE;
+  Launch L;
+  if ((rc = make_launch(stream, &L))) return rc;
+  if ((rc = mirror_address(host, &M))) return rc;
+  return launch_stream_resolve(L, M, C, slot_of_page, n_resident, page_table, max_pages, seq_lens, n_seqs,
+                               max_seq_len, dev_page_table, workspace);
+}
+
+int kv_stream_copy(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* pages, int32_t n, void* stream) {
+  CacheView C, M;
+  int rc = view_of(dev, &C);
+  if (rc) return rc;
+  if ((rc = mirror_of(host, C, &M))) return rc;
+  if (n < 0) return K8V4_EINVAL;
+  if (n == 0) return K8V4_OK;
+  if (!pages) return K8V4_EINVAL;
+  if (!aligned(pages, 8)) return K8V4_EALIGN;
+  Launch L;
+  if ((rc = make_launch(stream, &L))) return rc;
+  if ((rc = mirror_address(host, &M))) return rc;
+  return launch_stream_copy(L, M, C, pages, n);
 }
 
 int k8v4_last_device_status(void* stream) {

@@ -9,7 +9,10 @@
 // the unused half folded onto one pool) this is one fused kernel: one warp per
 // (token, KV head) loads K and V once, quantises K, rotates V exactly, quantises
 // it, and stores all four runs with vector stores (for short appends a warp pair
-// per (token, head) does the K and the V halves concurrently).
+// per (token, head) does the K and the V halves concurrently).  For a streamed
+// cache the same warp stores each row twice, to the host mirror page and to the
+// page's resident device slot (the streaming pull request's writers write both
+// copies, "How"), so the two copies cannot drift apart.
 //
 // The rotation is defined as the correctly rounded fp32 value of the exact
 // (H x) / 16.  The warp computes it with an int64 fixed-point fast Walsh-Hadamard
@@ -23,11 +26,15 @@ namespace {
 constexpr int kWarps = 8;
 
 // ------------------------------------------------------------------ append
-template <bool BF16, int FMT>
-__global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const int32_t* __restrict__ pt,
-                                                             int64_t max_pages, const int64_t* __restrict__ pos,
-                                                             int n_seqs, int n_tok, const void* __restrict__ k,
-                                                             const void* __restrict__ v, int split_kv, int* status) {
+// MIRROR: a streamed cache -- the page table holds host-mirror page ids; every
+// row goes to the mirror page M and, when slot_of_page says the page is
+// resident, to its device slot in C as well (one quantisation, two stores)
+template <bool BF16, int FMT, bool MIRROR>
+__global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, CacheView M, const int32_t* __restrict__ slot_of_page,
+                                                             const int32_t* __restrict__ pt, int64_t max_pages,
+                                                             const int64_t* __restrict__ pos, int n_seqs, int n_tok,
+                                                             const void* __restrict__ k, const void* __restrict__ v,
+                                                             int split_kv, int* status) {
   __shared__ long long stage[kWarps][kRotScratch];
   // a kernel launched after this one as a programmatic dependent (the decode
   // attention) may start its launch now; it waits for this grid's completion
@@ -51,13 +58,22 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, const 
   const int64_t pidx = cell / C.P;
   if (pidx >= max_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
   const int64_t page = pt[static_cast<int64_t>(b) * max_pages + pidx];
-  if (page < 0 || page >= C.n_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
   const int64_t r = (cell % C.P) * C.H + g;
-  uint8_t* base = C.pages + page * C.page_bytes;
   const int64_t elem = item * kD + 8 * lane;
-
-  if (role != 1) append_k_row<BF16, FMT>(C, base, r, k, elem, lane, stage[w]);
-  if (role != 0) append_v_row<BF16, FMT>(C, base, r, v, elem, lane, stage[w]);
+  uint8_t* base;
+  uint8_t* base2 = nullptr;
+  if (MIRROR) {
+    if (page < 0 || page >= M.n_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
+    base = M.pages + page * M.page_bytes;
+    const int slot = slot_of_page[page];
+    if (slot >= 0 && slot < C.n_pages) base2 = C.pages + static_cast<int64_t>(slot) * C.page_bytes;
+    else if (slot != -1 && lane == 0) record_status(status, K8V4_ERANGE);   // mirror written, slot skipped
+  } else {
+    if (page < 0 || page >= C.n_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
+    base = C.pages + page * C.page_bytes;
+  }
+  if (role != 1) append_k_row<BF16, FMT>(C, base, r, k, elem, lane, stage[w], base2);
+  if (role != 0) append_v_row<BF16, FMT>(C, base, r, v, elem, lane, stage[w], base2);
 }
 
 // ------------------------------------------------------------------ dequant
@@ -141,8 +157,17 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(CacheView C, const
 
 }  // namespace
 
+template <bool BF16, int FMT>
+void append_launch(const Launch& L, dim3 grid, dim3 block, const CacheView& C, const CacheView* M, const int32_t* slot,
+                   const int32_t* pt, int64_t max_pages, const int64_t* pos, int n_seqs, int n_tok, const void* k,
+                   const void* v, int split) {
+  if (M) append_kernel<BF16, FMT, true><<<grid, block, 0, L.stream>>>(C, *M, slot, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+  else append_kernel<BF16, FMT, false><<<grid, block, 0, L.stream>>>(C, C, nullptr, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+}
+
 int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_t max_pages, int n_seqs,
-                  const int64_t* pos, int n_tok, const void* k, const void* v, int dtype) {
+                  const int64_t* pos, int n_tok, const void* k, const void* v, int dtype, const CacheView* mirror,
+                  const int32_t* slot_of_page) {
   const int64_t items = static_cast<int64_t>(n_seqs) * n_tok * C.H;
   if (items == 0) return K8V4_OK;
   // short appends (up to a few thousand (token, head) items, e.g. a decode
@@ -152,15 +177,17 @@ int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_
   if (blocks > 0x7fffffffll) return K8V4_EINVAL;
   const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
   const bool bf = dtype == K8V4_BF16;
+  const CacheView* M = mirror;
+  const int32_t* so = slot_of_page;
   if (C.fmt == K8V4_FORMAT_K8V4) {
-    if (bf) append_kernel<true, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
-    else append_kernel<false, K8V4_FORMAT_K8V4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+    if (bf) append_launch<true, K8V4_FORMAT_K8V4>(L, grid, block, C, M, so, pt, max_pages, pos, n_seqs, n_tok, k, v, split);
+    else append_launch<false, K8V4_FORMAT_K8V4>(L, grid, block, C, M, so, pt, max_pages, pos, n_seqs, n_tok, k, v, split);
   } else if (C.fmt == K8V4_FORMAT_Q4) {
-    if (bf) append_kernel<true, K8V4_FORMAT_Q4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
-    else append_kernel<false, K8V4_FORMAT_Q4><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+    if (bf) append_launch<true, K8V4_FORMAT_Q4>(L, grid, block, C, M, so, pt, max_pages, pos, n_seqs, n_tok, k, v, split);
+    else append_launch<false, K8V4_FORMAT_Q4>(L, grid, block, C, M, so, pt, max_pages, pos, n_seqs, n_tok, k, v, split);
   } else {
-    if (bf) append_kernel<true, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
-    else append_kernel<false, K8V4_FORMAT_INT8><<<grid, block, 0, L.stream>>>(C, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+    if (bf) append_launch<true, K8V4_FORMAT_INT8>(L, grid, block, C, M, so, pt, max_pages, pos, n_seqs, n_tok, k, v, split);
+    else append_launch<false, K8V4_FORMAT_INT8>(L, grid, block, C, M, so, pt, max_pages, pos, n_seqs, n_tok, k, v, split);
   }
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
 }

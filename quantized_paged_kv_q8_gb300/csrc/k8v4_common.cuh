@@ -87,8 +87,18 @@ struct Launch {
   int num_sms;
 };
 
+// mirror != null: a streamed cache -- pt holds host-mirror page ids, every row is
+// written to the mirror and, where slot_of_page[page] >= 0, to that slot of C
 int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_t max_pages, int n_seqs,
-                  const int64_t* pos, int n_tok, const void* k, const void* v, int dtype);
+                  const int64_t* pos, int n_tok, const void* k, const void* v, int dtype,
+                  const CacheView* mirror = nullptr, const int32_t* slot_of_page = nullptr);
+// streamed caches: look up the pages the sequences read (resident slot, or a copy
+// from the host mirror M into a staging slot of C) and copy the misses
+int launch_stream_resolve(const Launch& L, const CacheView& M, const CacheView& C, const int32_t* slot_of_page,
+                          int n_resident, const int32_t* pt, int64_t max_pages, const int32_t* lens, int n_seqs,
+                          int max_seq_len, int32_t* dev_pt, void* ws);
+int launch_stream_copy(const Launch& L, const CacheView& M, const CacheView& C, const int32_t* pages, int n);
+size_t stream_ws_bytes(int n_seqs, int64_t max_pages);
 int launch_dequant(const Launch& L, const CacheView& C, const int32_t* pt, int64_t max_pages, int64_t start,
                    int64_t n_cells, float* k_out, float* v_rot_out, float* v_out);
 

@@ -268,10 +268,20 @@ __device__ __forceinline__ float quant_int8_half(const float x[8], uint2& packed
   return s;
 }
 
+// Stores of the row routines: every value goes to page `a` and, when `b` is
+// not null, to the same offset of page `b` (the host mirror of a streamed cache
+// and its resident device slot hold the same bytes)
+template <typename T>
+__device__ __forceinline__ void st2(uint8_t* a, uint8_t* b, int64_t off, T v) {
+  *reinterpret_cast<T*>(a + off) = v;
+  if (b != nullptr) *reinterpret_cast<T*>(b + off) = v;
+}
+
 // Q4_0 of the rotated vector (element 8 * lane + r; block = lane / 4).  Writes the
-// block's 16 nibble bytes (lanes 4b, 4b+1, 8 bytes each) and its fp16 scale
-// (lane 4b).
-__device__ __forceinline__ void quant_q4_store(const float y[8], int lane, uint8_t* vq, uint8_t* vs) {
+// block's 16 nibble bytes (lanes 4b, 4b+1, 8 bytes each) at q_off and its fp16
+// scale (lane 4b) at s_off of page a (and page b)
+__device__ __forceinline__ void quant_q4_store(const float y[8], int lane, uint8_t* a, uint8_t* b, int64_t q_off,
+                                               int64_t s_off) {
   uint32_t best = __float_as_uint(y[0]) & 0x7fffffffu;
   int bi = 0;
 #pragma unroll
@@ -311,46 +321,47 @@ __device__ __forceinline__ void quant_q4_store(const float y[8], int lane, uint8
       const uint32_t byte = ((packed >> (4 * r)) & 0xfu) | (((high >> (4 * r)) & 0xfu) << 4);
       out[r >> 2] |= byte << (8 * (r & 3));
     }
-    *reinterpret_cast<uint2*>(vq + 16 * blk + 8 * (lane & 1)) = make_uint2(out[0], out[1]);
+    st2(a, b, q_off + 16 * blk + 8 * (lane & 1), make_uint2(out[0], out[1]));
   }
-  if ((lane & 3) == 0) *reinterpret_cast<__half*>(vs + 2 * blk) = dh;
+  if ((lane & 3) == 0) st2(a, b, s_off + 2 * blk, dh);
 }
 
 // ------------------------------------------------------------------ row appends
 // K row of (token, head) r: int8 codes + two fp32 scales, or, in the Q4 format,
 // rotated q4_0 like V; ts is this warp's kRotScratch int64 of shared scratch
-// for the rotation (Q4 only)
+// for the rotation (Q4 only).  Written to page `base` and, when base2 is not
+// null, to page base2 as well.
 template <bool BF16, int FMT>
 __device__ __forceinline__ void append_k_row(const CacheView& C, uint8_t* base, int64_t r, const void* k, int64_t elem,
-                                             int lane, long long* ts) {
+                                             int lane, long long* ts, uint8_t* base2 = nullptr) {
   float x[8];
   load8<BF16>(k, elem, x);
   if (FMT == K8V4_FORMAT_Q4) {
     rotate_exact(x, lane, ts);
-    quant_q4_store(x, lane, base + r * 128, base + C.ks_off() + r * 16);
+    quant_q4_store(x, lane, base, base2, r * 128, C.ks_off() + r * 16);
     return;
   }
   uint2 kc;
   const float s = quant_int8_half(x, kc);
   const float s_hi = __shfl_xor_sync(kQFull, s, 16);
-  *reinterpret_cast<uint2*>(base + r * 256 + 8 * lane) = kc;
-  if (lane == 0) *reinterpret_cast<float2*>(base + C.ks_off() + r * 8) = make_float2(s, s_hi);
+  st2(base, base2, r * 256 + 8 * lane, kc);
+  if (lane == 0) st2(base, base2, C.ks_off() + r * 8, make_float2(s, s_hi));
 }
 // V row: rotated q4_0 (k8v4 and Q4) or int8 (the INT8 comparison format)
 template <bool BF16, int FMT>
 __device__ __forceinline__ void append_v_row(const CacheView& C, uint8_t* base, int64_t r, const void* v, int64_t elem,
-                                             int lane, long long* ts) {
+                                             int lane, long long* ts, uint8_t* base2 = nullptr) {
   float x[8];
   load8<BF16>(v, elem, x);
   if (FMT != K8V4_FORMAT_INT8) {
     rotate_exact(x, lane, ts);
-    quant_q4_store(x, lane, base + C.v_off() + r * 128, base + C.vs_off() + r * 16);
+    quant_q4_store(x, lane, base, base2, C.v_off() + r * 128, C.vs_off() + r * 16);
   } else {
     uint2 vc;
     const float sv = quant_int8_half(x, vc);
     const float sv_hi = __shfl_xor_sync(kQFull, sv, 16);
-    *reinterpret_cast<uint2*>(base + C.v_off() + r * 256 + 8 * lane) = vc;
-    if (lane == 0) *reinterpret_cast<float2*>(base + C.vs_off() + r * 8) = make_float2(sv, sv_hi);
+    st2(base, base2, C.v_off() + r * 256 + 8 * lane, vc);
+    if (lane == 0) st2(base, base2, C.vs_off() + r * 8, make_float2(sv, sv_hi));
   }
 }
 

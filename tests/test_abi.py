@@ -84,6 +84,30 @@ def test_bad_arguments_rejected(L):
     assert L.kv_dequant_k8v4(d, FAKE, 4, 60, 5, FAKE, FAKE, None, None) == k8.EINVAL
 
 
+def test_stream_arguments_rejected(L):
+    """The streaming calls check geometry, counts, pointers and sizes on the host."""
+    d, h = ctypes.byref(_desc()), ctypes.byref(_desc(pages=0x30000))
+    q4 = ctypes.byref(_desc(pages=0x30000, format=k8.FORMAT_Q4))
+    p32 = ctypes.byref(_desc(pages=0x30000, page_size=32))
+    assert L.kv_stream_workspace_bytes(2, 10) == 16 + 8 * 20
+    assert L.kv_stream_workspace_bytes(1, 1 << 29) == 0
+    args = (FAKE, 0, FAKE, 4, FAKE, 1, 64, FAKE, FAKE, 1 << 20, None)
+    assert L.kv_stream_resolve(q4, d, *args) == k8.EINVAL                # format differs
+    assert L.kv_stream_resolve(p32, d, *args) == k8.EINVAL               # page size differs
+    assert L.kv_stream_resolve(h, d, FAKE, 5, FAKE, 4, FAKE, 1, 64, FAKE, FAKE, 1 << 20, None) == k8.EINVAL
+    assert L.kv_stream_resolve(h, d, FAKE, 0, FAKE, 4, FAKE, 1, 65, FAKE, FAKE, 1 << 20, None) == k8.EINVAL
+    assert L.kv_stream_resolve(h, d, None, 0, FAKE, 4, FAKE, 1, 64, FAKE, FAKE, 1 << 20, None) == k8.EINVAL
+    assert L.kv_stream_resolve(h, d, FAKE, 0, FAKE, 4, FAKE, 1, 64, FAKE, FAKE, 47, None) == k8.ENOSPACE
+    assert L.kv_stream_resolve(h, d, FAKE, 0, FAKE, 4, FAKE, 1, 64, FAKE, ctypes.c_void_p(0x20008), 1 << 20,
+                               None) == k8.EALIGN
+    assert L.kv_stream_resolve(h, d, FAKE, 0, FAKE, 4, FAKE, 0, 64, FAKE, FAKE, 0, None) == k8.OK
+    assert L.kv_append_k8v4_mirrored(h, d, None, FAKE, 4, 1, FAKE, 1, FAKE, FAKE, k8.BF16, None) == k8.EINVAL
+    assert L.kv_append_k8v4_mirrored(q4, d, FAKE, FAKE, 4, 1, FAKE, 1, FAKE, FAKE, k8.BF16, None) == k8.EINVAL
+    assert L.kv_stream_copy(h, d, FAKE, -1, None) == k8.EINVAL
+    assert L.kv_stream_copy(h, d, ctypes.c_void_p(0x20004), 3, None) == k8.EALIGN
+    assert L.kv_stream_copy(h, d, FAKE, 0, None) == k8.OK
+
+
 def test_workspace_size_is_positive_and_monotone(L):
     d = ctypes.byref(_desc(n_pages=4096, page_size=64))
     a = L.attn_k8v4_workspace_bytes(d, 1, 1, 32768)

@@ -79,21 +79,26 @@ def peaks():
 
 
 def traffic_record(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    """DRAM bytes per launch from the committed ncu summary, or None when any
+    source file the kernel is built from changed since the counters were taken
+    (the summary lists the files and the first 16 hex digits of the SHA-256 of
+    their concatenation)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}_dram.txt")
     if not os.path.exists(path):
         return None
     fields = {}
     for line in open(path):
-        if ":" in line:
+        if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "quantized_paged_kv_q8_gb300", "csrc", fields.get("source", ""))
-    if not os.path.exists(src):
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != fields.get("source_sha256_16"):
+    h = hashlib.sha256()
+    for name in fields.get("source", "").split():
+        src = os.path.join(ROOT, "quantized_paged_kv_q8_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    if not fields.get("source") or h.hexdigest()[:16] != fields.get("source_sha256_16"):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
@@ -429,6 +434,8 @@ def main():
     ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify", "batched", "stream"],
                     help="lean single-kernel run for ncu (no replicas, INT8 arm, e2e or CPU baseline)")
     ap.add_argument("--chunk", type=int, default=8192, help="prefill chunk length (tokens)")
+    ap.add_argument("--format", default="k8v4", choices=["k8v4", "q4", "int8"],
+                    help="cache format of the --profile decode run")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -467,7 +474,8 @@ def main():
 
     # ---- bulk append (cache build) timing: append cells/s
     n_rep = 1 if args.profile else 2
-    caches = [k8.PagedCache(n_pages, P, H, device=dev) for _ in range(n_rep)]
+    fmt = {"k8v4": k8.FORMAT_K8V4, "q4": k8.FORMAT_Q4, "int8": k8.FORMAT_INT8}[args.format if args.profile else "k8v4"]
+    caches = [k8.PagedCache(n_pages, P, H, fmt=fmt, device=dev) for _ in range(n_rep)]
     for c in caches:
         k8.kv_append_k8v4(c, pt, zero, kd, vd)
     torch.cuda.synchronize()
@@ -533,8 +541,9 @@ def main():
 
     if args.profile:
         if rank == 0:
-            print(json.dumps({"profile": True, "ms_per_step": ms_step, "decode_ms": dec_ms,
-                              "gbs": CELL_BYTES * N_CELLS / (dec_ms / 1e3) / 1e9}), flush=True)
+            cb = caches[0].bytes_per_cell
+            print(json.dumps({"profile": True, "format": args.format, "ms_per_step": ms_step, "decode_ms": dec_ms,
+                              "gbs": cb * N_CELLS / (dec_ms / 1e3) / 1e9}), flush=True)
         return
 
     # ---- comparison formats on the same workload: INT8/INT8 (1,056 B/cell) and

@@ -140,3 +140,33 @@ def test_append_out_of_range_page_is_skipped_and_reported():
     ref.append(pt_ok, np.array([0]), k.f32[:, :32], v.f32[:, :32])
     ref.append(pt_ok, np.array([48]), k.f32[:, 48:], v.f32[:, 48:])
     _assert_bytes_equal(gpu, ref)
+
+
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_Q4])
+def test_append_rotation_fixed_point_edges(fmt):
+    """Rows whose values span exactly 23 and 24 bits in fixed point (sums
+    reaching 255 x (2^24 - 1) + 1), same-sign, negated and alternating-sign,
+    plus rows of 8-bit mantissas over 16 binades with one huge value: the exact
+    rotation's integer butterflies and its final rounding give the oracle's
+    bytes."""
+    n, P = 32, 16
+    rng = np.random.default_rng(77)
+    k = rng.standard_normal((1, n, 2, 256)).astype(np.float32)
+    v = rng.standard_normal((1, n, 2, 256)).astype(np.float32)
+    big23, big24 = float(2 ** 23 - 1), float(2 ** 24 - 1)
+    rows = []
+    for big in (big23, big24):
+        r = np.full(256, big, np.float32); r[5] = 1.0; rows.append(r)                 # all positive
+        rows.append(-rows[-1])                                                          # all negative
+        r = np.full(256, big, np.float32); r[1::2] *= -1; r[7] = 1.0; rows.append(r)  # alternating
+        r = (rng.integers(1, 2 ** 8, 256) * 2.0 ** rng.integers(0, 16, 256)).astype(np.float32)
+        r[3] = 1.0; r[4] = big; rows.append(r)                                          # mixed exponents
+    for i, r in enumerate(rows):
+        v[0, i, i % 2] = r
+        k[0, 16 + i, i % 2] = r
+    pt = np.random.default_rng(6).permutation(n // P)[None].astype(np.int32)
+    gpu, ref = make_caches(n // P, P, 2, fmt)
+    append_both(gpu, ref, pt, np.array([0]), synth.Tensor(k, "f32"), synth.Tensor(v, "f32"))
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    _assert_bytes_equal(gpu, ref)

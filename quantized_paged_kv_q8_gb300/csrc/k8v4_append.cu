@@ -34,7 +34,8 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, CacheV
                                                              const int32_t* __restrict__ pt, int64_t max_pages,
                                                              const int64_t* __restrict__ pos, int n_seqs, int n_tok,
                                                              const void* __restrict__ k, const void* __restrict__ v,
-                                                             int split_kv, int* status) {
+                                                             int split_kv, FastDiv div_h, FastDiv div_tok, FastDiv div_p,
+                                                             int* status) {
   __shared__ long long stage[kWarps][kRotScratch];
   // a kernel launched after this one as a programmatic dependent (the decode
   // attention) may start its launch now; it waits for this grid's completion
@@ -44,30 +45,33 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, CacheV
   // (seq, token, head) per warp, or, for short appends (a decode step's token),
   // (seq, token, head, half): warp pairs split a (token, head) into its K half
   // (int8 quantisation; rotation + q4_0 in the Q4 format) and its V half
-  // (rotation + q4_0, or int8), which run concurrently
+  // (rotation + q4_0, or int8), which run concurrently.  The host keeps every
+  // warp index below 2^31, and a cell that passes the range check is below
+  // max_pages * P <= 2^31, so the index arithmetic runs in 32 bits.
   const int64_t wi = static_cast<int64_t>(blockIdx.x) * kWarps + w;
   const int64_t total = static_cast<int64_t>(n_seqs) * n_tok * C.H;
   if (wi >= (split_kv ? 2 * total : total)) return;
   const int role = split_kv ? static_cast<int>(wi & 1) : 2;             // 0: K only, 1: V only, 2: both
-  const int64_t item = split_kv ? wi >> 1 : wi;                         // (seq, token, head)
-  const int g = static_cast<int>(item % C.H);
-  const int64_t it = item / C.H;
-  const int b = static_cast<int>(it / n_tok), t = static_cast<int>(it % n_tok);
+  const uint32_t item = static_cast<uint32_t>(split_kv ? wi >> 1 : wi);  // (seq, token, head)
+  const uint32_t it = div_h.div(item);
+  const int g = static_cast<int>(item - it * static_cast<uint32_t>(C.H));
+  const uint32_t b = div_tok.div(it);
+  const int t = static_cast<int>(it - b * static_cast<uint32_t>(n_tok));
   const int64_t cell = pos[b] + t;
-  if (cell < 0) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
-  const int64_t pidx = cell / C.P;
-  if (pidx >= max_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
+  if (cell < 0 || cell >= max_pages * C.P) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
+  const uint32_t pidx = div_p.div(static_cast<uint32_t>(cell));
+  const int cslot = static_cast<int>(static_cast<uint32_t>(cell) - pidx * static_cast<uint32_t>(C.P));
   const int64_t page = pt[static_cast<int64_t>(b) * max_pages + pidx];
-  const int64_t r = (cell % C.P) * C.H + g;
-  const int64_t elem = item * kD + 8 * lane;
+  const int64_t r = static_cast<int64_t>(cslot) * C.H + g;
+  const int64_t elem = static_cast<int64_t>(item) * kD + 8 * lane;
   uint8_t* base;
   uint8_t* base2 = nullptr;
   if (MIRROR) {
     if (page < 0 || page >= M.n_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
     base = M.pages + page * M.page_bytes;
-    const int slot = slot_of_page[page];
-    if (slot >= 0 && slot < C.n_pages) base2 = C.pages + static_cast<int64_t>(slot) * C.page_bytes;
-    else if (slot != -1 && lane == 0) record_status(status, K8V4_ERANGE);   // mirror written, slot skipped
+    const int dslot = slot_of_page[page];
+    if (dslot >= 0 && dslot < C.n_pages) base2 = C.pages + static_cast<int64_t>(dslot) * C.page_bytes;
+    else if (dslot != -1 && lane == 0) record_status(status, K8V4_ERANGE);   // mirror written, slot skipped
   } else {
     if (page < 0 || page >= C.n_pages) { if (lane == 0) record_status(status, K8V4_ERANGE); return; }
     base = C.pages + page * C.page_bytes;
@@ -161,8 +165,9 @@ template <bool BF16, int FMT>
 void append_launch(const Launch& L, dim3 grid, dim3 block, const CacheView& C, const CacheView* M, const int32_t* slot,
                    const int32_t* pt, int64_t max_pages, const int64_t* pos, int n_seqs, int n_tok, const void* k,
                    const void* v, int split) {
-  if (M) append_kernel<BF16, FMT, true><<<grid, block, 0, L.stream>>>(C, *M, slot, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
-  else append_kernel<BF16, FMT, false><<<grid, block, 0, L.stream>>>(C, C, nullptr, pt, max_pages, pos, n_seqs, n_tok, k, v, split, L.status);
+  const FastDiv dh(static_cast<uint32_t>(C.H)), dt(static_cast<uint32_t>(n_tok)), dp(static_cast<uint32_t>(C.P));
+  if (M) append_kernel<BF16, FMT, true><<<grid, block, 0, L.stream>>>(C, *M, slot, pt, max_pages, pos, n_seqs, n_tok, k, v, split, dh, dt, dp, L.status);
+  else append_kernel<BF16, FMT, false><<<grid, block, 0, L.stream>>>(C, C, nullptr, pt, max_pages, pos, n_seqs, n_tok, k, v, split, dh, dt, dp, L.status);
 }
 
 int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_t max_pages, int n_seqs,
@@ -173,8 +178,8 @@ int launch_append(const Launch& L, const CacheView& C, const int32_t* pt, int64_
   // short appends (up to a few thousand (token, head) items, e.g. a decode
   // step) take a warp pair per item for latency; long ones a warp per item
   const int split = items * 2 <= static_cast<int64_t>(L.num_sms) * 16 ? 1 : 0;
+  if ((split ? 2 : 1) * items >= (int64_t(1) << 31)) return K8V4_EINVAL;   // warp indices stay below 2^31
   const int64_t blocks = ((split ? 2 : 1) * items + kWarps - 1) / kWarps;
-  if (blocks > 0x7fffffffll) return K8V4_EINVAL;
   const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
   const bool bf = dtype == K8V4_BF16;
   const CacheView* M = mirror;

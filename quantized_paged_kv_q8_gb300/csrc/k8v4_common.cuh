@@ -46,6 +46,22 @@ struct CacheView {
   }
 };
 
+// ---------------------------------------------------------------- division
+// Division by a kernel-invariant divisor d >= 1 for dividends below 2^31, by the
+// round-up multiply-high method: s = ceil(log2 d), m = floor(2^32 (2^s - d) / d)
+// + 1, q = (umulhi(n, m) + n) >> s (exact for every n < 2^31; the sum stays
+// below 2^32).  Three instructions instead of a 64-bit division routine.
+struct FastDiv {
+  uint32_t d = 1, m = 1;
+  int s = 0;
+  FastDiv() = default;
+  __host__ explicit FastDiv(uint32_t div) : d(div) {
+    while ((1ull << s) < d) ++s;
+    m = static_cast<uint32_t>(((1ull << 32) * ((1ull << s) - d)) / d + 1);
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> s; }
+};
+
 // ---------------------------------------------------------------- status word
 // Kernels record the first device-side error here (compare-and-swap from 0) and
 // skip the offending access; the host reads and clears it.

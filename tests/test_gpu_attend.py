@@ -235,3 +235,37 @@ def test_decode_bad_length_and_page_are_reported():
     decode_gpu(gpu, q, torch.from_numpy(bad).cuda(), w.seq_lens, 256)
     assert k8.k8v4_last_device_status() == k8.ERANGE
     assert np.all(gpu.pages.cpu().numpy() == ref.buf)
+
+
+@pytest.mark.parametrize("fmt,H", [(k8.FORMAT_K8V4, 1), (k8.FORMAT_K8V4, 3), (k8.FORMAT_Q4, 3), (k8.FORMAT_INT8, 3)])
+def test_other_kv_head_counts(fmt, H):
+    """1 and 3 KV heads (8 and 24 query heads), 32-cell pages, two sequences in
+    one interleaved pool: cache bytes equal the oracle's and decode and verify
+    are within the tolerance (the index arithmetic divides by H, P and the
+    token count; 3 is the first divisor that is not a power of two)."""
+    seed = synth.config_seed(2) + 40 + H
+    P = 32
+    lens = np.array([1111, 300], np.int32)
+    pt, n_pages = synth.interleaved_pool(seed, lens, P)
+    ks = [synth.kv_values(seed, synth.T_K, b, int(n), H, 3, "bf16") for b, n in enumerate(lens)]
+    vs = [synth.kv_values(seed, synth.T_V, b, int(n), H, 3, "bf16") for b, n in enumerate(lens)]
+    gpu, ref = make_caches(n_pages, P, H, fmt)
+    for b in range(len(lens)):
+        append_both(gpu, ref, pt[b:b + 1], np.array([0]), synth.Tensor(ks[b].f32[None], "bf16"),
+                    synth.Tensor(vs[b].f32[None], "bf16"))
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    assert np.array_equal(gpu.pages.cpu().numpy(), ref.buf)
+    pt_d = torch.from_numpy(pt).cuda()
+    HQ = 8 * H
+    q = synth.q_values(seed, 0, len(lens), H, "bf16")
+    got = decode_gpu(gpu, dev_tensor(q, (len(lens), HQ, 256)), pt_d, lens, int(lens.max()))
+    rs, rh, rv = oracle.decode_rows(len(lens), HQ, lens)
+    assert rel_err(got.reshape(-1, 256), ref.attention(pt, rs, rh, rv, q.f32.reshape(-1, 256))) <= TOL
+    steps = np.stack([np.maximum(int(L) - 4 + np.arange(5), 0) for L in lens]).astype(np.int32)
+    qs = [synth.q_values(seed, 1 + b, 5, H, "bf16") for b in range(len(lens))]
+    got = verify_gpu(gpu, torch.stack([dev_tensor(x) for x in qs]), pt_d, steps, int(lens.max()))
+    assert k8.k8v4_last_device_status() == 0
+    rs, rh, rv = oracle.multi_query_rows(steps, HQ)
+    qrows = np.concatenate([x.f32.reshape(-1, 256) for x in qs])
+    assert rel_err(got.reshape(-1, 256), ref.attention(pt, rs, rh, rv, qrows)) <= TOL

@@ -576,17 +576,21 @@ def main():
     int8_arm = format_arm(k8.FORMAT_INT8, CELL_BYTES_INT8)
     q4_arm = format_arm(k8.FORMAT_Q4, CELL_BYTES_Q4)
 
-    # ---- end to end through the C ABI with host buffers
-    q_h = q.cpu().pin_memory()
-    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    # ---- end to end through the C ABI with host buffers: the step's inputs
+    # travel as one pinned buffer (q | k_new | v_new, bf16; every part starts on a
+    # 16-byte boundary), one host -> device copy per step, and the output comes
+    # back with one device -> host copy
+    nq, nk = q.numel(), k_new.numel()
+    in_h = torch.cat([q.reshape(-1), k_new.reshape(-1), v_new.reshape(-1)]).cpu().pin_memory()
+    in_s = torch.empty(in_h.shape, dtype=in_h.dtype, device=dev)
+    q_s = in_s[:nq].view(q.shape)
+    kn_s = in_s[nq:nq + nk].view(k_new.shape)
+    vn_s = in_s[nq + nk:].view(v_new.shape)
     out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    q_s, kn_s, vn_s = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
     Ke = max(20, min(K, 2000))
 
     def e2e_step(i):
-        q_s.copy_(q_h, non_blocking=True)
-        kn_s.copy_(kn_h, non_blocking=True)
-        vn_s.copy_(vn_h, non_blocking=True)
+        in_s.copy_(in_h, non_blocking=True)
         k8.attn_k8v4_decode_step(caches[i % n_rep], q_s, kn_s, vn_s, pt, lens, N_CELLS, out, wsp)
         out_h.copy_(out, non_blocking=True)
 
@@ -600,7 +604,7 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
-    h2d = q.numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2
+    h2d = in_h.numel() * in_h.element_size()
     d2h = out.numel() * 4
 
     del caches, kd, vd

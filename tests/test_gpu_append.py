@@ -5,7 +5,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import quantized_paged_kv_q8_gb300 as k8
 import synth
 from gpu_util import CANARY, append_both, dev_tensor, make_caches

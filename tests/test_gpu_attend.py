@@ -8,7 +8,7 @@ import torch
 import oracle
 import quantized_paged_kv_q8_gb300 as k8
 import synth
-from gpu_util import CANARY, TOL, append_both, decode_gpu, dev_tensor, make_caches, rel_err, verify_gpu
+from gpu_util import TOL, append_both, decode_gpu, dev_tensor, make_caches, rel_err, verify_gpu
 
 pytestmark = pytest.mark.gpu
 

@@ -9,7 +9,7 @@ import torch
 import oracle
 import quantized_paged_kv_q8_gb300 as k8
 import synth
-from gpu_util import TOL, append_both, dev_tensor, make_caches, rel_err
+from gpu_util import TOL, dev_tensor, make_caches, rel_err
 
 pytestmark = pytest.mark.gpu
 

@@ -6,7 +6,6 @@ printed on the pages, or a hand-derived fixture under tests/golden/.  A plausibl
 mistake anywhere in the oracle (a dropped term, a wrong sign or index, a swapped
 operand, a wrong tie rule) fails at least one of them.
 """
-import math
 import os
 from fractions import Fraction
 

@@ -607,3 +607,62 @@ def test_stream_resolve_reads_the_right_bytes(orc):
                     assert np.array_equal(dev_mem[dev[b, i]], host[pt[b, i]])
                 else:
                     assert dev[b, i] == -1
+
+
+@pytest.mark.parametrize("fmt", ["k8v4", "int8", "q4"])
+def test_head_count_separability(orc, fmt):
+    """A cache of 3 KV heads agrees head by head with three 1-head caches of the
+    same rows (same page table, same bytes per head, same dequantised values),
+    and its attention rows for query head h equal those of the 1-head cache of
+    KV head h // 8: the (slot, head) interleaving and the GQA map hold for any
+    head count."""
+    f = {"k8v4": orc.FMT_K8V4, "int8": orc.FMT_INT8, "q4": orc.FMT_Q4}[fmt]
+    rng = np.random.default_rng(21)
+    n, P, H = 45, 8, 3
+    n_pages = (n + P - 1) // P
+    pt = rng.permutation(n_pages + 2)[:n_pages].astype(np.int32)[None]
+    k = rng.standard_normal((1, n, H, D)).astype(np.float32)
+    v = rng.standard_normal((1, n, H, D)).astype(np.float32)
+    v[..., 5] *= 20
+    big = orc.Cache(n_pages + 2, P, H, f)
+    big.append(pt, np.array([0]), k, v)
+    kb, vb, ob = big.dequant(pt, 0, n)
+    q = rng.standard_normal((8 * H, D)).astype(np.float32)
+    rs, rh, rv = orc.decode_rows(1, 8 * H, [n])
+    att = big.attention(pt, rs, rh, rv, q)
+    chb = orc.bytes_per_cell_head(f)
+    for g in range(H):
+        one = orc.Cache(n_pages + 2, P, 1, f)
+        one.append(pt, np.array([0]), k[:, :, g:g + 1], v[:, :, g:g + 1])
+        k1, v1, o1 = one.dequant(pt, 0, n)
+        assert np.array_equal(k1[:, 0], kb[:, g]) and np.array_equal(v1[:, 0], vb[:, g])
+        assert np.array_equal(o1[:, 0], ob[:, g])
+        r1s, r1h, r1v = orc.decode_rows(1, 8, [n])
+        att1 = one.attention(pt, r1s, r1h, r1v, q[8 * g:8 * g + 8])
+        assert np.array_equal(att1, att[8 * g:8 * g + 8])
+        # byte runs: every run of (cell, head g) in the big page equals the
+        # 1-head page's run, at offsets scaled by H
+        for c in (0, 9, n - 1):
+            page = int(pt[0, c // P])
+            pb_big, pb_one = P * H * chb, P * chb
+            slot = c % P
+            big_page = big.buf[page * pb_big:(page + 1) * pb_big]
+            one_page = one.buf[page * pb_one:(page + 1) * pb_one]
+            run_off, off1 = 0, 0
+            for run in orc_runs(f):
+                a = big_page[run_off * H * P + (slot * H + g) * run: run_off * H * P + (slot * H + g + 1) * run]
+                b = one_page[off1 * P + slot * run: off1 * P + (slot + 1) * run]
+                assert np.array_equal(a, b), (fmt, g, c, run)
+                run_off += run
+                off1 += run
+
+
+def orc_runs(fmt_code):
+    """Bytes per (cell, head) of each run of a format, in page order (K, K
+    scales, V, V scales), from the layout the pages describe."""
+    import oracle
+    if fmt_code == oracle.FMT_K8V4:
+        return (256, 8, 128, 16)
+    if fmt_code == oracle.FMT_INT8:
+        return (256, 8, 256, 8)
+    return (128, 16, 128, 16)

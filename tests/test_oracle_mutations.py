@@ -1,0 +1,74 @@
+"""The oracle's pins catch plausible mistakes: each case below plants one
+mistake in a copy of the oracle's C source (on the CPU, in a temporary build),
+loads that build in place of the real one, and runs the pins; at least one pin
+must fail.  The real oracle is restored afterwards."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = open(oracle.SRC).read()
+
+# (name, text in k8v4_oracle.c, replacement): one plausible mistake each
+MUTATIONS = [
+    ("int8 ties away from zero", "float r = rintf(x[i] / s);", "float r = roundf(x[i] / s);"),
+    ("int8 divisor 128", "float s = a / 127.0f;", "float s = a / 128.0f;"),
+    ("q4 last index on ties", "if (fabsf(y[j]) > fabsf(y[im])) im = j;", "if (fabsf(y[j]) >= fabsf(y[im])) im = j;"),
+    ("q4 scale sign", "orc_f32_to_f16(m / -8.0f)", "orc_f32_to_f16(m / 8.0f)"),
+    ("q4 ties away from zero", "float r = rintf(y[j] / d) + 8.0f;", "float r = roundf(y[j] / d) + 8.0f;"),
+    ("nibble order", "nib[j] = (uint8_t)(q[j] | (q[j + 16] << 4));", "nib[j] = (uint8_t)((q[j] << 4) | q[j + 16]);"),
+    ("hadamard index", "__builtin_popcount((unsigned)(i & j))", "__builtin_popcount((unsigned)(i | j))"),
+    ("V run offset", "p.vq = base + 264 * H * P + r * 128;", "p.vq = base + 256 * H * P + r * 128;"),
+    ("GQA map", "g = h / GQA;", "g = h % a->C.H;"),
+    ("softmax scale dropped", "sc[j] = dot * a->sm_scale;", "sc[j] = dot;"),
+    ("inverse rotation scale", "o[i] = s / 16.0;", "o[i] = s / 8.0;"),
+    ("one cell short", "n = a->row_vis[r], g", "n = a->row_vis[r] - (a->row_vis[r] > 0), g"),
+]
+
+PINS = [
+    lambda o: pins.test_int8_hand_ties(o),
+    lambda o: pins.test_int8_bound_and_extremes(o),
+    lambda o: pins.test_q4_hand_ties_through_rotation(o),
+    lambda o: pins.test_q4_error_bounds(o),
+    lambda o: pins.test_hadamard_is_sylvester_and_orthogonal(o),
+    lambda o: pins.test_rotate_equals_exact_rational_rounding(o, "normal"),
+    lambda o: pins.test_page_layout_hand_offsets(o),
+    lambda o: pins.test_attention_closed_forms(o),
+    lambda o: pins.test_attention_matches_torch_sdpa(o, "k8v4"),
+    lambda o: pins.test_head_count_separability(o, "k8v4"),
+]
+
+
+def _build(tmp_path, text: str) -> str:
+    src = os.path.join(tmp_path, "mutant.c")
+    lib = os.path.join(tmp_path, "libmutant.so")
+    with open(src, "w") as f:
+        f.write(text)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", lib, src, "-lm"], check=True)
+    return lib
+
+
+def test_unmutated_oracle_passes_the_pins():
+    oracle.build()
+    for pin in PINS:
+        pin(oracle)
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_the_mutation(tmp_path, monkeypatch, name, old, new):
+    assert SRC.count(old) == 1, f"mutation target not found once: {old}"
+    lib = _build(str(tmp_path), SRC.replace(old, new))
+    monkeypatch.setattr(oracle, "LIB", lib)
+    monkeypatch.setattr(oracle, "build", lambda force=False: lib)
+    monkeypatch.setattr(oracle, "_lib", None)
+    caught = []
+    for i, pin in enumerate(PINS):
+        try:
+            pin(oracle)
+        except Exception:                     # an assertion, or an error the mistake provokes
+            caught.append(i)
+            break
+    assert caught, f"no pin failed for the mutation '{name}'"

@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes: each case below plants one
-mistake in a copy of the oracle's C source (on the CPU, in a temporary build),
-loads that build in place of the real one, and runs the pins; at least one pin
-must fail.  The real oracle is restored afterwards."""
+mistake in a copy of the oracle's C source (on the CPU, in a temporary build)
+or of its Python page-lookup function, puts it in place of the real one, and
+runs the pins; at least one pin must fail.  The real oracle is restored
+afterwards."""
 import os
 import subprocess
 
@@ -26,6 +27,8 @@ MUTATIONS = [
     ("softmax scale dropped", "sc[j] = dot * a->sm_scale;", "sc[j] = dot;"),
     ("inverse rotation scale", "o[i] = s / 16.0;", "o[i] = s / 8.0;"),
     ("one cell short", "n = a->row_vis[r], g", "n = a->row_vis[r] - (a->row_vis[r] > 0), g"),
+    ("q4 K left rotated", "orc_hadamard_rotate(kr, k_out + off);", "memcpy(k_out + off, kr, sizeof kr);"),
+    ("q4 query rotation scale", "q[i] = s / 16.0;", "q[i] = s / 8.0;"),
 ]
 
 PINS = [
@@ -39,6 +42,8 @@ PINS = [
     lambda o: pins.test_attention_closed_forms(o),
     lambda o: pins.test_attention_matches_torch_sdpa(o, "k8v4"),
     lambda o: pins.test_head_count_separability(o, "k8v4"),
+    lambda o: pins.test_q4_format_quantises_k_like_v(o),
+    lambda o: pins.test_q4_format_dequant_and_attention(o),
 ]
 
 
@@ -70,5 +75,48 @@ def test_pins_catch_the_mutation(tmp_path, monkeypatch, name, old, new):
             pin(oracle)
         except Exception:                     # an assertion, or an error the mistake provokes
             caught.append(i)
+            break
+    assert caught, f"no pin failed for the mutation '{name}'"
+
+
+# ---------------------------------------------------------------- the lookup oracle (Python)
+STREAM_SRC = None
+
+
+def _stream_variant(old: str, new: str):
+    """oracle.stream_resolve with one line of its source replaced."""
+    import inspect
+    import textwrap
+    global STREAM_SRC
+    if STREAM_SRC is None:
+        STREAM_SRC = textwrap.dedent(inspect.getsource(oracle.stream_resolve))
+    assert STREAM_SRC.count(old) == 1, old
+    ns = {"np": __import__("numpy")}
+    exec(STREAM_SRC.replace(old, new), ns)
+    return ns["stream_resolve"]
+
+
+STREAM_MUTATIONS = [
+    ("pages rounded down", "for i in range((n + P - 1) // P):", "for i in range(n // P):"),
+    ("lengths not clipped", "n = min(max(int(seq_lens[b]), 0), max_seq_len)", "n = max(int(seq_lens[b]), 0)"),
+    ("staging from n_resident + 1", "slot = n_resident + rank", "slot = n_resident + rank + 1"),
+]
+
+STREAM_PINS = [
+    lambda o: pins.test_stream_resolve_worked_example(o),
+    lambda o: pins.test_stream_resolve_extremes_and_overflow(o),
+    lambda o: pins.test_stream_resolve_reads_the_right_bytes(o),
+]
+
+
+@pytest.mark.parametrize("name,old,new", STREAM_MUTATIONS, ids=[m[0] for m in STREAM_MUTATIONS])
+def test_stream_pins_catch_the_mutation(monkeypatch, name, old, new):
+    monkeypatch.setattr(oracle, "stream_resolve", _stream_variant(old, new))
+    caught = False
+    for pin in STREAM_PINS:
+        try:
+            pin(oracle)
+        except Exception:
+            caught = True
             break
     assert caught, f"no pin failed for the mutation '{name}'"

@@ -124,3 +124,17 @@ def test_valid_call_without_gpu_reports_device(L):
     d = ctypes.byref(_desc())
     assert L.kv_append_k8v4(d, FAKE, 4, 1, FAKE, 1, FAKE, FAKE, k8.BF16, None) in (k8.EDEVICE, k8.ECUDA)
     assert k8.status_string(k8.ERANGE).startswith("position")
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/k8v4.h compiles as C99 with warnings as errors, and every entry
+    point the binding exports is declared there with a C prototype."""
+    import subprocess
+    names = k8.EXPORTED
+    src = tmp_path / "use_header.c"
+    body = "\n".join(f"  (void)&{n};" for n in names)
+    src.write_text(f'#include "k8v4.h"\nint main(void) {{\n{body}\n  return 0;\n}}\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc, "-c", str(src),
+                        "-o", str(tmp_path / "use_header.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -17,6 +17,9 @@ SRC = open(oracle.SRC).read()
 MUTATIONS = [
     ("int8 ties away from zero", "float r = rintf(x[i] / s);", "float r = roundf(x[i] / s);"),
     ("int8 divisor 128", "float s = a / 127.0f;", "float s = a / 128.0f;"),
+    ("int8 reciprocal quotient", "float r = rintf(x[i] / s);", "float r = rintf(x[i] * (1.0f / s));"),
+    ("int8 quotient by absmax", "float r = rintf(x[i] / s);", "float r = rintf((x[i] * 127.0f) / a);"),
+    ("q4 reciprocal quotient", "float r = rintf(y[j] / d) + 8.0f;", "float r = rintf(y[j] * (1.0f / d)) + 8.0f;"),
     ("q4 last index on ties", "if (fabsf(y[j]) > fabsf(y[im])) im = j;", "if (fabsf(y[j]) >= fabsf(y[im])) im = j;"),
     ("q4 scale sign", "orc_f32_to_f16(m / -8.0f)", "orc_f32_to_f16(m / 8.0f)"),
     ("q4 ties away from zero", "float r = rintf(y[j] / d) + 8.0f;", "float r = roundf(y[j] / d) + 8.0f;"),
@@ -33,6 +36,8 @@ MUTATIONS = [
 
 PINS = [
     lambda o: pins.test_int8_hand_ties(o),
+    lambda o: pins.test_int8_quotient_is_one_ieee_division(o),
+    lambda o: pins.test_q4_quotient_is_one_ieee_division(o),
     lambda o: pins.test_int8_bound_and_extremes(o),
     lambda o: pins.test_q4_hand_ties_through_rotation(o),
     lambda o: pins.test_q4_error_bounds(o),

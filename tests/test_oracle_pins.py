@@ -192,6 +192,43 @@ def test_int8_bound_and_extremes(orc):
     assert s == 0.0 and not c.any()
 
 
+def _read_quotient_golden(name):
+    """Rows of int8_quotient.txt / q4_quotient.txt: the fp32 inputs (exact hex)
+    and, per reading of the quotient, the code it gives."""
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        fields = [f.split() for f in line.split("|")]
+        vals = [float.fromhex(t) for t in fields[0]]
+        codes = [int(f[0]) for f in fields[1:]]
+        rows.append((vals, codes))
+    return rows
+
+
+def test_int8_quotient_is_one_ieee_division(orc):
+    """Codes that tell x / s apart from x * (1 / s) and from (x * 127) / a (the
+    PR's "INT8 rules with ties-to-even" fix the rounding of the code; the
+    quotient is read as one correctly rounded fp32 division).  Each fixture line
+    was derived with exact rational arithmetic; a non-power-of-two absmax makes
+    the three readings differ."""
+    rows = _read_quotient_golden("int8_quotient.txt")
+    assert len(rows) >= 8
+    recip_differs = absmax_differs = 0
+    for (a, x, s), (code, code_recip, code_absmax) in rows:
+        # the fixture's own consistency, checked exactly
+        assert Fraction(s) == _round_to_f32(Fraction(a) / 127)
+        recip_differs += code_recip != code
+        absmax_differs += code_absmax != code
+        half = np.zeros(128, np.float32)
+        half[0], half[1] = a, x
+        c, got_s = orc.quant_int8(half)
+        assert got_s == s
+        assert int(c[0]) == 127 and int(c[1]) == code, (a, x, int(c[1]), code)
+    assert recip_differs >= 4 and absmax_differs >= 4
+
+
 # ----------------------------------------------------------------------------- Q4_0
 
 def _read_q4_golden():
@@ -231,6 +268,23 @@ def test_q4_hand_ties_through_rotation(orc):
         other = (blk + 1) % 8
         nib0, d0 = orc.quant_q4_block(yr[32 * other:32 * other + 32])
         assert d0 == 0x8000 and np.all(nib0 == 0x88)
+
+
+def test_q4_quotient_is_one_ieee_division(orc):
+    """Q4_0 codes that tell y / d apart from y * (1 / d): blocks whose fp16
+    scale d has a non-power-of-two significand, with y next to a half-integer
+    multiple of d (fixture derived with exact rational arithmetic)."""
+    rows = _read_quotient_golden("q4_quotient.txt")
+    assert len(rows) >= 6
+    for (m, y, d), (code, code_recip) in rows:
+        assert code_recip != code
+        blk = np.zeros(32, np.float32)
+        blk[0], blk[1] = m, y
+        nib, db = orc.quant_q4_block(blk)
+        assert db == int(np.float16(d).view(np.uint16)) and float(np.float16(d)) == d
+        codes = np.concatenate([nib & 15, nib >> 4])
+        assert codes[0] == 0 and codes[1] == code, (m, y, int(codes[1]), code)
+        assert np.all(codes[2:] == 8)
 
 
 def test_q4_error_bounds(orc):

@@ -24,6 +24,10 @@
  *    skipped (never dereferenced) and recorded in a device status word that
  *    k8v4_last_device_status() returns.  No kernel traps or spins.
  *  - The library never calls exit() and never throws across the ABI.
+ *  - At its first call on a device the library looks up, with that device
+ *    current, the device addresses of its own device variables (the status
+ *    word below) and keeps them for the life of the process; do not use the
+ *    library on a device after cudaDeviceReset() on it.
  *  - Query head h reads KV head h / 8 (GQA group of 8 query heads).
  *
  * Page layout (per page of P cells and H KV heads; r = slot * H + head):
@@ -181,7 +185,10 @@ int attn_k8v4_decode_step(const k8v4_cache* cache, const void* q, int32_t q_dtyp
  * first call before any stream capture.  All calls share the one array: calls
  * that overlap on the GPU (other streams, other host threads) race and corrupt
  * each other's results, so serialise them.  Nothing in the array has to start
- * at zero: each call writes every partial it reads. */
+ * at zero: each call writes every partial it reads.  The looked-up address is
+ * kept for the life of the process: after cudaDeviceReset() on a device the
+ * cached address is stale, so do not call this entry point on that device
+ * again in the same process. */
 int attn_k8v4_decode_noalloc(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                              int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
                              float sm_scale, float* out, void* stream);

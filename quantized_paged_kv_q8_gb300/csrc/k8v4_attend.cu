@@ -36,22 +36,14 @@ namespace k8v4 {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-#ifndef K8V4_STAGES
-#define K8V4_STAGES 3
-#endif
-#ifndef K8V4_QF_SMEM
-#define K8V4_QF_SMEM 0       // 1: q fragments live in shared memory instead of registers
-#endif
-#ifndef K8V4_DECODE_WARPS
-#define K8V4_DECODE_WARPS 8
-#endif
-constexpr int kStages = K8V4_STAGES;          // cp.async stages per tile group
-constexpr int kWarps = K8V4_DECODE_WARPS;     // warps per CTA (tile groups x queries)
+constexpr int kStages = 3;      // cp.async stages per tile group
+constexpr int kWarps = 8;       // warps per CTA (tile groups x queries)
 constexpr int kPStride = 260;   // floats per partial row: o[256], m, l, 2 pad
-#ifndef K8V4_PV_PLANES
-#define K8V4_PV_PLANES 3
-#endif
-constexpr int kPlanes = K8V4_PV_PLANES;   // bf16 terms of p * d (3 = 24 significant bits)
+// bf16 terms of p * d: three give 24 significant bits, the precision the
+// element-wise error budget of the decode paths is derived for; fewer terms
+// would leave the budget
+constexpr int kPlanes = 3;
+static_assert(kPlanes == 3, "p * d must be carried in three bf16 terms");
 
 template <int FMT>
 struct Stage {
@@ -412,14 +404,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
       }
     }
   }
-#if K8V4_QF_SMEM
-  // per-warp q fragments after the tile-group stages: [8 pairs of k-steps][32 lanes] x 16 B
-  uint4* qsm = reinterpret_cast<uint4*>(smem + static_cast<size_t>(p.n_groups) * kStages * S::kBytes) + warp * 8 * 32;
-#pragma unroll
-  for (int kp = 0; kp < 8; ++kp)
-    qsm[kp * 32 + lane] = make_uint4(qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
-  __syncwarp();
-#endif
   // score factors for the heads of the C layout (2c, 2c+1): held by lanes 4h
   const float f0 = __shfl_sync(kFull, fscale, 8 * c), f1 = __shfl_sync(kFull, fscale, 8 * c + 4);
 
@@ -549,18 +533,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
           codes_to_f16(wa[j], a[j][0], a[j][2]);
           codes_to_f16(wb[j], a[j][1], a[j][3]);
         }
-#if K8V4_QF_SMEM
-        const uint4 qa = qsm[(2 * i) * 32 + lane], qb = qsm[(2 * i + 1) * 32 + lane];
-        const uint32_t qq[4][2] = {{qa.x, qa.y}, {qa.z, qa.w}, {qb.x, qb.y}, {qb.z, qb.w}};
-#endif
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float* dst = acc[2 * (i >> 1) + (j & 1)];
-#if K8V4_QF_SMEM
-          mma_f16(dst, a[j], qq[j][0], qq[j][1]);
-#else
           mma_f16(dst, a[j], qf[4 * i + j][0], qf[4 * i + j][1]);
-#endif
           if (QF32) mma_f16(dst, a[j], qf_lo[(4 * i + j) % (kLo ? 16 : 1)][0], qf_lo[(4 * i + j) % (kLo ? 16 : 1)][1]);
         }
       }
@@ -801,8 +777,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) attend_splitk_kernel(const Att
 
 template <int FMT, bool QF32, bool NQ1>
 int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, float* out) {
-  const size_t stage_bytes = static_cast<size_t>(plan.n_groups) * kStages * Stage<FMT>::kBytes +
-                             (K8V4_QF_SMEM ? static_cast<size_t>(plan.warps) * 8 * 32 * 16 : 0);
+  const size_t stage_bytes = static_cast<size_t>(plan.n_groups) * kStages * Stage<FMT>::kBytes;
   const size_t merge_bytes = static_cast<size_t>(plan.warps) * (8 * 256 + 16) * sizeof(float);
   const size_t smem = stage_bytes > merge_bytes ? stage_bytes : merge_bytes;
   auto kern = attend_splitk_kernel<FMT, QF32, NQ1>;

@@ -733,12 +733,10 @@ AttendPlan plan_verify_tc(const CacheView& C, int n_seqs, int n_q, int max_seq_l
   // many short CTAs (one resident per SM at a time): the block scheduler hands
   // the next split to whichever SM frees up, so sequences of unequal length
   // balance out and the tail is one short CTA; at least two CTAs per SM
-#ifndef K8V4_VERIFY_TILES_PER_SPLIT
-#define K8V4_VERIFY_TILES_PER_SPLIT 16
-#endif
+  constexpr int kTilesPerSplit = 16;
   const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
   int64_t splits = std::max<int64_t>((2ll * num_sms + pairs - 1) / pairs,
-                                     (tiles + K8V4_VERIFY_TILES_PER_SPLIT - 1) / K8V4_VERIFY_TILES_PER_SPLIT);
+                                     (tiles + kTilesPerSplit - 1) / kTilesPerSplit);
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, tiles));
   const int tps = static_cast<int>((tiles + splits - 1) / splits);
   pl.cells_per_split = kTileN * tps;

@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libk8v4.so")
-SOURCES = ["k8v4_api.cu", "k8v4_append.cu", "k8v4_attend.cu", "k8v4_verify.cu", "k8v4_combine.cu", "k8v4_prefill.cu", "k8v4_noalloc.cu",
+SOURCES = ["k8v4_api.cu", "k8v4_append.cu", "k8v4_attend.cu", "k8v4_decode.cu", "k8v4_verify.cu", "k8v4_combine.cu", "k8v4_prefill.cu", "k8v4_noalloc.cu",
            "k8v4_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -813,6 +813,7 @@ AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len,
     tc.ws_bytes = std::max(tc.ws_bytes, mw.ws_bytes);
     return tc;
   }
+  if (n_q == 1 && decode_ws_supported(C)) return plan_decode(C, n_seqs, max_seq_len, num_sms);
   AttendPlan pl{};
   pl.n_q = n_q;
   pl.n_groups = n_q >= kWarps ? 1 : kWarps / n_q;
@@ -845,6 +846,9 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
     const AttendPlan mw = plan_verify(C, n_seqs, plan.n_q, max_seq_len, L.num_sms);
     return launch_verify(L, C, mw, q, q_dtype, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
   }
+  if (plan.n_q == 1 && decode_ws_supported(C))
+    return launch_decode(L, C, plan, q, q_dtype, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws,
+                         k_new, v_new, kv_dtype, 0);
   AttendParams p;
   p.C = C;
   p.q = q;

@@ -137,6 +137,14 @@ AttendPlan plan_verify_tc(const CacheView& C, int n_seqs, int n_q, int max_seq_l
 int launch_verify_tc(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q,
                      const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
                      float sm_scale, float* out, void* ws);
+// the warp-specialised TMA decode kernel (k8v4_decode.cu): one query per
+// sequence over the K8V4 or INT8 format; spin = mbarrier poll limit (0: default)
+bool decode_ws_supported(const CacheView& C);
+AttendPlan plan_decode(const CacheView& C, int n_seqs, int max_seq_len, int num_sms);
+int launch_decode(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
+                  const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
+                  float sm_scale, float* out, void* ws, const void* k_new, const void* v_new, int kv_dtype,
+                  uint32_t spin);
 // weighted sum of split partials (o[256], m, l rows of 260 floats) -> out, launched programmatically dependent
 int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out);
 int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,

@@ -193,6 +193,46 @@ int attn_k8v4_decode_noalloc(const k8v4_cache* cache, const void* q, int32_t q_d
                              int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
                              float sm_scale, float* out, void* stream);
 
+/* ---------------------------------------------------------------- split across GPUs
+ * One long sequence's decode split by cell range over several GPUs (the path
+ * the k8v4 PR's engine runs with its multi-GPU split, header: "Rebased on
+ * v0.1.21 (the multi-GPU layer split)"): GPU r attends over its cells
+ * [cell_begin_r, cell_end_r) with attn_k8v4_decode_partial, the partial rows of
+ * all GPUs are exchanged (an all-gather of n_seqs * 8H * 260 floats per GPU),
+ * and every GPU merges them with attn_k8v4_combine_partials.  The merged result
+ * is the decode output over the union of the ranges.
+ *
+ * Partial row layout (260 floats per (sequence, query head)): o[256], the
+ * un-rotated softmax-weighted sum of V relative to 2^m; m, a base-2 exponent at
+ * least the row's largest sm_scale * log2(e) * q . Khat over the range (-inf
+ * when the range holds no visible cell); l, the sum of 2^(score - m); two
+ * unused floats.  For ranges r the output is
+ *   sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r,  M = max_r m_r. */
+
+/* Workspace bytes attn_k8v4_decode_partial needs for a range of cell_end -
+ * cell_begin cells; 0 for a format other than K8V4 or INT8 or a bad range. */
+size_t attn_k8v4_partial_workspace_bytes(const k8v4_cache* cache, int32_t n_seqs, int32_t cell_begin,
+                                         int32_t cell_end);
+
+/* Decode attention of each sequence's query over its cells [cell_begin,
+ * min(cell_end, seq_lens[b])), written as partial rows.
+ *   partial:    float [n_seqs][8*H][260], 16-byte aligned (layout above).
+ *   cell_begin: a multiple of 16; cell_end >= cell_begin, a multiple of 16 or
+ *               >= max_seq_len.
+ *   workspace:  >= attn_k8v4_partial_workspace_bytes(cache, n_seqs, cell_begin,
+ *               cell_end) bytes, 256-byte aligned.
+ * Other arguments as attn_k8v4_decode.  K8V4 and INT8 formats. */
+int attn_k8v4_decode_partial(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
+                             int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
+                             int32_t cell_begin, int32_t cell_end, float sm_scale, float* partial, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Merge gathered partial rows parts[n_parts][n_seqs][n_rows][260] (device)
+ * into out[n_seqs][n_rows][256] (device, float): for each row the weighted sum
+ * above; a row whose parts all have m = -inf outputs zeros. */
+int attn_k8v4_combine_partials(const float* parts, int32_t n_parts, int32_t n_seqs, int32_t n_rows, float* out,
+                               void* stream);
+
 /* Verify attention: n_q queries per sequence, query i of sequence b seeing
  * step_arrays[b][i] cells (the batched form with per-query step arrays, as
  * verify uses it, the k8v4 PR "Tests"; for a speculative window of 4 drafts + 1
@@ -283,6 +323,16 @@ int kv_stream_resolve(const k8v4_cache* host, const k8v4_cache* dev, const int32
  * resident window).  pages: int32 [n][2] (device), 8-byte aligned.  An id out of
  * range is recorded (K8V4_ERANGE) and its copy skipped. */
 int kv_stream_copy(const k8v4_cache* host, const k8v4_cache* dev, const int32_t* pages, int32_t n, void* stream);
+
+/* Failure-handling diagnostics: the bound, in nanoseconds, of every mbarrier
+ * wait in the kernels that use them (TMA-fed decode, tensor-memory prefill and
+ * verify); 0 restores each kernel's default (about one second), and a bound
+ * under 1000 ns means a single poll with no waiting.  A wait that runs out
+ * records K8V4_ECUDA, the kernel releases what it holds and returns; a tiny
+ * bound therefore makes such a call fail without harm (the copies and MMAs it
+ * already issued are still waited for, with the default bound), which is how
+ * the recovery path is tested.  Process-wide; not for production use. */
+void k8v4_set_wait_limit_ns(uint32_t ns);
 
 /* Synchronise `stream`, return the first device-side error recorded since the
  * last call (K8V4_OK if none) and clear it.  The word is per device and shared

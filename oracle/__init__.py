@@ -69,6 +69,8 @@ def lib():
             L.orc_dequant.restype = I
             L.orc_attention.argtypes = [P, I, I, I, P, I64, I64, P, P, P, P, Dd, P, I, I]
             L.orc_attention.restype = I
+            L.orc_attention_partial.argtypes = [P, I, I, I, P, I64, I64, P, P, P, P, P, Dd, P, P, P, I]
+            L.orc_attention_partial.restype = I
             _lib = L
     return _lib
 
@@ -191,6 +193,27 @@ class Cache:
                             _ptr(rh), _ptr(rv), _ptr(q), float(sm_scale), _ptr(out), int(rotate_back),
                             n_threads or n_threads_default())
         return out
+
+
+    def attention_partial(self, page_table: np.ndarray, row_seq, row_head, row_lo, row_hi, q_rows: np.ndarray,
+                          sm_scale: float = 1.0 / 16.0, n_threads: int | None = None):
+        """fp64 partial attention over cells [row_lo, row_hi) per row: (o, m, l)
+        with o un-rotated and unnormalised, m the natural-log maximum score."""
+        pt = np.ascontiguousarray(page_table, dtype=np.int32)
+        if pt.ndim == 1:
+            pt = pt[None]
+        rs, rh = np.ascontiguousarray(row_seq, np.int32), np.ascontiguousarray(row_head, np.int32)
+        lo, hi = np.ascontiguousarray(row_lo, np.int32), np.ascontiguousarray(row_hi, np.int32)
+        q = np.ascontiguousarray(q_rows, dtype=np.float32).reshape(-1, D)
+        n = rs.shape[0]
+        assert rh.shape[0] == n and lo.shape[0] == n and hi.shape[0] == n and q.shape[0] == n
+        o = np.empty((n, D), np.float64)
+        m = np.empty(n, np.float64)
+        lsum = np.empty(n, np.float64)
+        lib().orc_attention_partial(_ptr(self.buf), self.fmt, self.P, self.H, _ptr(pt), pt.shape[1], n, _ptr(rs),
+                                    _ptr(rh), _ptr(lo), _ptr(hi), _ptr(q), float(sm_scale), _ptr(o), _ptr(m),
+                                    _ptr(lsum), n_threads or n_threads_default())
+        return o, m, lsum
 
 
 def stream_resolve(page_table: np.ndarray, seq_lens, slot_of_page, n_resident: int, n_dev_pages: int, P: int,

@@ -466,12 +466,14 @@ typedef struct {
   int rotate_back;
 } attn_ctx;
 
-static void attn_row(void* vctx, int64_t r) {
-  attn_ctx* a = (attn_ctx*)vctx;
-  int b = a->row_seq[r], h = a->row_head[r], n = a->row_vis[r], g = h / GQA;
-  const float* q32 = a->q + r * D;
+/* Attention of one query row over cells [lo, hi) of sequence b, KV head g:
+ * the scores s_j = (q . Khat_j) sm_scale, their maximum m and the sum l of
+ * exp(s_j - m); acc = sum_j exp(s_j - m) Vhat_rot_j, divided by l when `norm`
+ * (0 for an empty range); o = (H/16) acc when `rotate_back`, else acc. */
+static void range_attention(const cache_t* C, int b, int g, int lo, int hi, const float* q32, double sm_scale,
+                            int norm, int rotate_back, double* o, double* m_out, double* l_out) {
   double q[D];
-  if (a->C.fmt == ORC_FMT_Q4) {          /* (H/16) q: scores against Khat_rot */
+  if (C->fmt == ORC_FMT_Q4) {            /* (H/16) q: scores against Khat_rot */
     for (int i = 0; i < D; ++i) {
       double s = 0.0;
       for (int j = 0; j < D; ++j) s += hadamard_sign(i, j) * (double)q32[j];
@@ -480,28 +482,29 @@ static void attn_row(void* vctx, int64_t r) {
   } else {
     for (int i = 0; i < D; ++i) q[i] = (double)q32[i];
   }
-  double* o = a->out + r * D;
+  int n = hi > lo ? hi - lo : 0;
   double* sc = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
   double acc[D];
   float kh[D], vh[D];
   memset(acc, 0, sizeof acc);
   double mx = -INFINITY;
   for (int j = 0; j < n; ++j) {
-    read_cell(&a->C, b, j, g, kh, vh);
+    read_cell(C, b, lo + j, g, kh, vh);
     double dot = 0.0;
     for (int i = 0; i < D; ++i) dot += q[i] * (double)kh[i];
-    sc[j] = dot * a->sm_scale;
+    sc[j] = dot * sm_scale;
     if (sc[j] > mx) mx = sc[j];
   }
   double l = 0.0;
   for (int j = 0; j < n; ++j) {
     double p = exp(sc[j] - mx);
     l += p;
-    read_cell(&a->C, b, j, g, kh, vh);
+    read_cell(C, b, lo + j, g, kh, vh);
     for (int i = 0; i < D; ++i) acc[i] += p * (double)vh[i];
   }
-  for (int i = 0; i < D; ++i) acc[i] = n > 0 ? acc[i] / l : 0.0;
-  if (a->rotate_back) {
+  if (norm)
+    for (int i = 0; i < D; ++i) acc[i] = n > 0 ? acc[i] / l : 0.0;
+  if (rotate_back) {
     for (int i = 0; i < D; ++i) {
       double s = 0.0;
       for (int j = 0; j < D; ++j) s += hadamard_sign(i, j) * acc[j];
@@ -510,7 +513,47 @@ static void attn_row(void* vctx, int64_t r) {
   } else {
     memcpy(o, acc, sizeof acc);
   }
+  *m_out = mx;
+  *l_out = l;
   free(sc);
+}
+
+static void attn_row(void* vctx, int64_t r) {
+  attn_ctx* a = (attn_ctx*)vctx;
+  int b = a->row_seq[r], h = a->row_head[r], n = a->row_vis[r], g = h / GQA;
+  double m, l;
+  range_attention(&a->C, b, g, 0, n, a->q + r * D, a->sm_scale, 1, a->rotate_back, a->out + r * D, &m, &l);
+}
+
+/* Partial attention over a cell range (the cell-range split of one decode
+ * across GPUs): for row r, cells [row_lo[r], row_hi[r]) of its sequence,
+ *   m = max_j s_j,  l = sum_j exp(s_j - m),  o = (H/16) sum_j exp(s_j - m) Vhat_rot_j
+ * (natural exponent; o un-rotated and unnormalised); an empty range gives
+ * m = -inf, l = 0, o = 0.  Merging ranges: out = sum_r e^(m_r - M) o_r /
+ * sum_r e^(m_r - M) l_r. */
+typedef struct {
+  cache_t C;
+  const int32_t *row_seq, *row_head, *row_lo, *row_hi;
+  const float* q;
+  double sm_scale;
+  double *o, *m, *l;
+} part_ctx;
+
+static void part_row(void* vctx, int64_t r) {
+  part_ctx* a = (part_ctx*)vctx;
+  const int b = a->row_seq[r], h = a->row_head[r];
+  const int kv = h / GQA;                 /* query head h reads KV head h / 8 */
+  range_attention(&a->C, b, kv, a->row_lo[r], a->row_hi[r], a->q + r * D, a->sm_scale, 0,
+                  a->C.fmt != ORC_FMT_INT8, a->o + r * D, a->m + r, a->l + r);
+}
+
+int orc_attention_partial(const uint8_t* pages, int fmt, int P, int H, const int32_t* pt, int64_t max_pages,
+                          int64_t n_rows, const int32_t* row_seq, const int32_t* row_head, const int32_t* row_lo,
+                          const int32_t* row_hi, const float* q, double sm_scale, double* o, double* m, double* l,
+                          int n_threads) {
+  part_ctx a = {{(uint8_t*)pages, fmt, P, H, pt, max_pages}, row_seq, row_head, row_lo, row_hi, q, sm_scale, o, m, l};
+  parallel_for(n_threads, n_rows, part_row, &a);
+  return 0;
 }
 
 /* One output row per (sequence, head, visible count): out[r] = softmax-weighted

@@ -69,6 +69,10 @@ def lib():
             "kv_stream_workspace_bytes": ([I32, I64], SZ),
             "kv_stream_resolve": ([C, C, P, I32, P, I64, P, I32, I32, P, P, SZ, P], ctypes.c_int),
             "kv_stream_copy": ([C, C, P, I32, P], ctypes.c_int),
+            "attn_k8v4_partial_workspace_bytes": ([C, I32, I32, I32], SZ),
+            "attn_k8v4_decode_partial": ([C, P, I32, P, I64, P, I32, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
+            "attn_k8v4_combine_partials": ([P, I32, I32, I32, P, P], ctypes.c_int),
+            "k8v4_set_wait_limit_ns": ([ctypes.c_uint32], None),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -83,7 +87,9 @@ EXPORTED = ("k8v4_bytes_per_cell", "k8v4_status_string", "k8v4_device_check", "k
             "attn_k8v4_verify",
             "attn_k8v4_prefill",
             "kv_dequant_k8v4", "k8v4_last_device_status",
-            "kv_append_k8v4_mirrored", "kv_stream_workspace_bytes", "kv_stream_resolve", "kv_stream_copy")
+            "kv_append_k8v4_mirrored", "kv_stream_workspace_bytes", "kv_stream_resolve", "kv_stream_copy",
+            "attn_k8v4_partial_workspace_bytes", "attn_k8v4_decode_partial", "attn_k8v4_combine_partials",
+            "k8v4_set_wait_limit_ns")
 
 
 def status_string(code: int) -> str:
@@ -265,3 +271,88 @@ def kv_stream_copy(host: PagedCache, dev: PagedCache, pages: torch.Tensor, strea
 
 def k8v4_last_device_status(stream=None) -> int:
     return int(lib().k8v4_last_device_status(_stream(stream)))
+
+
+# ---------------------------------------------------------------- split across GPUs
+PARTIAL_ROW = 260      # floats per partial row: o[256], m (base-2 exponent), l, 2 unused
+
+
+def cell_ranges(max_seq_len: int, world: int, align: int = 16) -> list[tuple[int, int]]:
+    """Split cells [0, max_seq_len) into `world` contiguous ranges of whole
+    16-cell tiles, as even as the tiles allow; the last range ends at
+    max_seq_len (possibly past a shorter sequence's length, which is fine)."""
+    assert world >= 1 and max_seq_len >= 0
+    tiles = (max_seq_len + align - 1) // align
+    bounds = [align * ((tiles * r) // world) for r in range(world)] + [max_seq_len]
+    return [(min(bounds[r], max_seq_len), bounds[r + 1] if r + 1 < world else max_seq_len) for r in range(world)]
+
+
+def attn_k8v4_partial_workspace_bytes(cache: PagedCache, n_seqs: int, cell_begin: int, cell_end: int) -> int:
+    return int(lib().attn_k8v4_partial_workspace_bytes(cache.ref(), n_seqs, cell_begin, cell_end))
+
+
+def partial_workspace(cache: PagedCache, n_seqs: int, cell_begin: int, cell_end: int, device="cuda") -> torch.Tensor:
+    n = attn_k8v4_partial_workspace_bytes(cache, n_seqs, cell_begin, cell_end)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def attn_k8v4_decode_partial(cache: PagedCache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                             max_seq_len: int, cell_begin: int, cell_end: int, partial: torch.Tensor,
+                             ws: torch.Tensor, sm_scale: float = 1.0 / 16.0, stream=None) -> torch.Tensor:
+    """Decode over cells [cell_begin, cell_end) only; partial: float32
+    [n_seqs, 8H, 260] (o[256] unnormalised, m, l)."""
+    assert q.is_contiguous() and partial.is_contiguous() and partial.dtype == torch.float32
+    assert partial.shape[-1] == PARTIAL_ROW
+    rc = lib().attn_k8v4_decode_partial(cache.ref(), _ptr(q), _dtype(q), _ptr(page_table), page_table.shape[-1],
+                                        _ptr(seq_lens), q.shape[0], max_seq_len, cell_begin, cell_end, sm_scale,
+                                        _ptr(partial), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "attn_k8v4_decode_partial")
+    return partial
+
+
+def attn_k8v4_combine_partials(parts: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """parts: float32 [n_parts, n_seqs, rows, 260] -> out float32 [n_seqs, rows, 256]."""
+    assert parts.is_contiguous() and out.is_contiguous() and parts.dtype == torch.float32
+    n_parts, n_seqs, rows = parts.shape[0], parts.shape[1], parts.shape[2]
+    assert parts.shape[3] == PARTIAL_ROW and tuple(out.shape) == (n_seqs, rows, HEAD_DIM)
+    rc = lib().attn_k8v4_combine_partials(_ptr(parts), n_parts, n_seqs, rows, _ptr(out), _stream(stream))
+    _check(rc, "attn_k8v4_combine_partials")
+    return out
+
+
+def decode_across_ranks(cache: PagedCache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                        max_seq_len: int, out: torch.Tensor, group=None, sm_scale: float = 1.0 / 16.0,
+                        stream=None) -> torch.Tensor:
+    """Decode split by cell range across the ranks of `group` (one GPU each,
+    every rank holding the same cache layout and page table): rank r attends
+    over its range of cell_ranges(max_seq_len, world), the partial rows are
+    all-gathered (n_seqs * 8H * 260 floats per rank), and every rank merges
+    them into `out`."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    lo, hi = cell_ranges(max_seq_len, world)[rank]
+    n_seqs, rows = q.shape[0], q.shape[1]
+    part = torch.empty(n_seqs, rows, PARTIAL_ROW, dtype=torch.float32, device=q.device)
+    ws = partial_workspace(cache, n_seqs, lo, hi, device=q.device)
+    attn_k8v4_decode_partial(cache, q, page_table, seq_lens, max_seq_len, lo, hi, part, ws, sm_scale, stream)
+    return attn_k8v4_combine_partials(gather_partials(part, group), out, stream)
+
+
+def gather_partials(part: torch.Tensor, group=None) -> torch.Tensor:
+    """The exchange step of the cell-range split: every rank's partial rows
+    [n_seqs, rows, 260] stacked in rank order, [world, n_seqs, rows, 260]
+    (an all-gather; any torch.distributed backend, NCCL on GPUs)."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    parts = torch.empty((world,) + tuple(part.shape), dtype=part.dtype, device=part.device)
+    if world > 1:
+        dist.all_gather(list(parts.unbind(0)), part.contiguous(), group=group)
+    else:
+        parts[0].copy_(part)
+    return parts
+
+
+def k8v4_set_wait_limit_ns(ns: int) -> None:
+    """Failure-handling diagnostics: bound of every mbarrier wait (0: default)."""
+    lib().k8v4_set_wait_limit_ns(int(ns))

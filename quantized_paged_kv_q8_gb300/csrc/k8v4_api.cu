@@ -1,5 +1,6 @@
 // The extern "C" entry points declared in include/k8v4.h: host-side argument
 // validation, the per-device status word, and the launches.
+#include <atomic>
 #include <mutex>
 
 #include "k8v4_common.cuh"
@@ -21,6 +22,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+std::atomic<uint32_t> g_wait_ns{0};       // 0: each kernel's default bound
 
 // Per-device set-up, done once with the device current: check that it is an
 // sm_103 part and find the device address of the status word.
@@ -110,6 +112,9 @@ int mirror_address(const k8v4_cache* host, CacheView* M) {
 }
 
 }  // namespace
+
+uint32_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 }  // namespace k8v4
 
 using namespace k8v4;
@@ -213,6 +218,58 @@ int attn_k8v4_verify(const k8v4_cache* cache, const void* q, int32_t q_dtype, co
   return attend_common(cache, q, q_dtype, page_table, max_pages, step_arrays, n_seqs, n_q, max_seq_len, sm_scale, out,
                        workspace, workspace_bytes, stream);
 }
+
+size_t attn_k8v4_partial_workspace_bytes(const k8v4_cache* cache, int32_t n_seqs, int32_t cell_begin,
+                                         int32_t cell_end) {
+  CacheView C;
+  if (view_of(cache, &C) != K8V4_OK || !decode_ws_supported(C)) return 0;
+  if (n_seqs < 0 || cell_begin < 0 || cell_end < cell_begin) return 0;
+  DeviceState* s = nullptr;
+  const int sms = device_state(&s) == K8V4_OK ? s->num_sms : 152;
+  return plan_decode(C, n_seqs, cell_end - cell_begin, sms).ws_bytes;
+}
+
+int attn_k8v4_decode_partial(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
+                             int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
+                             int32_t cell_begin, int32_t cell_end, float sm_scale, float* partial, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  CacheView C;
+  int rc = view_of(cache, &C);
+  if (rc) return rc;
+  if (!decode_ws_supported(C)) return K8V4_EINVAL;
+  if ((rc = check_table(C, page_table, max_pages))) return rc;
+  if (n_seqs < 0 || n_seqs > 65535) return K8V4_EINVAL;
+  if (q_dtype != K8V4_F32 && q_dtype != K8V4_BF16) return K8V4_EINVAL;
+  if (max_seq_len < 0 || static_cast<int64_t>(max_seq_len) > max_pages * C.P) return K8V4_EINVAL;
+  if (cell_begin < 0 || cell_begin % 16 != 0 || cell_end < cell_begin) return K8V4_EINVAL;
+  if (cell_end % 16 != 0 && cell_end < max_seq_len) return K8V4_EINVAL;
+  if (!(sm_scale > 0.0f) || sm_scale > 1e30f) return K8V4_EINVAL;
+  if (n_seqs == 0) return K8V4_OK;
+  if (!q || !seq_lens || !partial || !workspace) return K8V4_EINVAL;
+  if (!aligned(q, 16) || !aligned(partial, 16) || !aligned(workspace, 256) || !aligned(seq_lens, 4))
+    return K8V4_EALIGN;
+  Launch L;
+  if ((rc = make_launch(stream, &L))) return rc;
+  const AttendPlan plan = plan_decode(C, n_seqs, cell_end - cell_begin, L.num_sms);
+  if (workspace_bytes < plan.ws_bytes) return K8V4_ENOSPACE;
+  return launch_decode_partial(L, C, plan, q, q_dtype, page_table, max_pages, seq_lens, n_seqs, max_seq_len,
+                               cell_begin, cell_end, sm_scale, partial, workspace, wait_limit_ns());
+}
+
+int attn_k8v4_combine_partials(const float* parts, int32_t n_parts, int32_t n_seqs, int32_t n_rows, float* out,
+                               void* stream) {
+  if (n_parts < 1 || n_parts > (1 << 20) || n_seqs < 0 || n_rows < 1 || n_rows > 4096) return K8V4_EINVAL;
+  if (static_cast<int64_t>(n_seqs) * n_rows > (int64_t(1) << 31) - 1) return K8V4_EINVAL;
+  if (n_seqs == 0) return K8V4_OK;
+  if (!parts || !out) return K8V4_EINVAL;
+  if (!aligned(parts, 16) || !aligned(out, 16)) return K8V4_EALIGN;
+  Launch L;
+  int rc = make_launch(stream, &L);
+  if (rc) return rc;
+  return launch_combine_parts(L, parts, n_parts, n_seqs, n_rows, out);
+}
+
+void k8v4_set_wait_limit_ns(uint32_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
 
 int attn_k8v4_prefill(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                       int64_t max_pages, int32_t seq_len, int32_t n_q_tok, const int32_t* step_arrays, float sm_scale,

@@ -848,7 +848,7 @@ int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, c
   }
   if (plan.n_q == 1 && decode_ws_supported(C))
     return launch_decode(L, C, plan, q, q_dtype, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws,
-                         k_new, v_new, kv_dtype, 0);
+                         k_new, v_new, kv_dtype, wait_limit_ns());
   AttendParams p;
   p.C = C;
   p.q = q;

@@ -1,6 +1,9 @@
-// Combine of the split-K partials of decode and verify: each split wrote, per
-// output row, its un-rotated o[256] together with its running maximum m (log2
-// domain) and sum l; the row's result is sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// Combine of split-K partials: each split (or, for the cell-range split across
+// GPUs, each rank) wrote, per output row, its un-rotated o[256] together with
+// its running maximum m (base-2 exponent) and sum l; the row's result is
+// sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.  The same kernel can instead
+// write the merged partial itself (o, M, L unnormalised), which is what one GPU
+// of a cell-range split hands to the others.
 //
 // One CTA per (row, 32-dim chunk), eight warps.  Warp w folds splits w, w + 8,
 // ... into a running (M, L, acc) with the online-softmax update, so every load
@@ -15,23 +18,23 @@ namespace {
 
 constexpr int kPStride = 260;   // floats per partial row: o[256], m, l, 2 pad
 
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws, int splits, int n_q, int HQ,
-                                                      float* __restrict__ out) {
+// row r = (b, rr) with rr < rows_per_b; split s of row r at
+// src + b * b_stride + s * split_stride + rr * kPStride
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ src, int splits, int64_t split_stride,
+                                                      int64_t b_stride, int rows_per_b, float* __restrict__ out,
+                                                      int write_partial) {
   __shared__ float wm[8], wl[8], wacc[8][32];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int row = blockIdx.x, chunk = blockIdx.y;   // row = (b, qi, head)
-  const int head = row % HQ;
-  const int bq = row / HQ;
-  const int b = bq / n_q, qi = bq % n_q;
-  const int64_t stride = static_cast<int64_t>(n_q) * HQ * kPStride;     // between splits
-  const float* base = ws + ((static_cast<int64_t>(b) * splits * n_q + qi) * HQ + head) * kPStride;
+  const int row = blockIdx.x, chunk = blockIdx.y;
+  const int b = row / rows_per_b, rr = row % rows_per_b;
+  const float* base = src + b * b_stride + static_cast<int64_t>(rr) * kPStride;
   const int dim = chunk * 32 + lane;
   float M = -INFINITY, L = 0.0f, acc = 0.0f;
 #pragma unroll 4
   for (int s = warp; s < splits; s += 8) {
-    const float* src = base + s * stride;
-    const float ms = src[256], ls = src[257], x = src[dim];
+    const float* p = base + s * split_stride;
+    const float ms = p[256], ls = p[257], x = p[dim];
     if (ms == -INFINITY) continue;                     // nothing visible in this split
     const float mn = fmaxf(M, ms);
     const float a = exp2f(M - mn), w = exp2f(ms - mn);  // a = 0 while M = -inf
@@ -59,14 +62,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         Lt += wl[w] * f;
       }
     }
-    out[static_cast<int64_t>(row) * kD + dim] = Lt > 0.0f ? v / Lt : 0.0f;
+    if (write_partial) {
+      float* dst = out + static_cast<int64_t>(row) * kPStride;
+      dst[dim] = v;
+      if (chunk == 0 && lane == 0) {
+        dst[256] = Mt;
+        dst[257] = Lt;
+        dst[258] = 0.0f;
+        dst[259] = 0.0f;
+      }
+    } else {
+      out[static_cast<int64_t>(row) * kD + dim] = Lt > 0.0f ? v / Lt : 0.0f;
+    }
   }
 }
 
-}  // namespace
-
-int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out) {
-  const int rows = n_seqs * n_q * H * kGqa;
+int launch(const Launch& L, const float* src, int splits, int64_t split_stride, int64_t b_stride, int n_seqs,
+           int rows_per_b, float* out, int write_partial) {
+  const int rows = n_seqs * rows_per_b;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows, kD / 32);
   cfg.blockDim = dim3(256);
@@ -77,8 +90,30 @@ int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel, ws, splits, n_q, H * kGqa, out) != cudaSuccess) return K8V4_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, combine_kernel, src, splits, split_stride, b_stride, rows_per_b, out, write_partial) !=
+      cudaSuccess)
+    return K8V4_ECUDA;
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
+}
+
+}  // namespace
+
+int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out) {
+  const int rows_per_b = n_q * H * kGqa;
+  const int64_t split_stride = static_cast<int64_t>(rows_per_b) * kPStride;
+  return launch(L, ws, splits, split_stride, split_stride * splits, n_seqs, rows_per_b, out, 0);
+}
+
+int launch_combine_partial(const Launch& L, const float* ws, int splits, int n_seqs, int H, float* partial) {
+  const int rows_per_b = H * kGqa;
+  const int64_t split_stride = static_cast<int64_t>(rows_per_b) * kPStride;
+  return launch(L, ws, splits, split_stride, split_stride * splits, n_seqs, rows_per_b, partial, 1);
+}
+
+int launch_combine_parts(const Launch& L, const float* parts, int n_parts, int n_seqs, int n_rows_per_seq,
+                         float* out) {
+  const int64_t b_stride = static_cast<int64_t>(n_rows_per_seq) * kPStride;
+  return launch(L, parts, n_parts, b_stride * n_seqs, b_stride, n_seqs, n_rows_per_seq, out, 0);
 }
 
 }  // namespace k8v4

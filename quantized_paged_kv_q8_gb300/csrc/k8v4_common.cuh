@@ -145,8 +145,22 @@ int launch_decode(const Launch& L, const CacheView& C, const AttendPlan& plan, c
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
                   float sm_scale, float* out, void* ws, const void* k_new, const void* v_new, int kv_dtype,
                   uint32_t spin);
+// cells [cell_begin, cell_end) of every sequence only, merged into unnormalised
+// partial rows [n_seqs][8 H][260] (o[256], m as a base-2 exponent, l); the plan
+// is plan_decode over cell_end - cell_begin cells
+int launch_decode_partial(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
+                          const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs,
+                          int max_seq_len, int cell_begin, int cell_end, float sm_scale, float* partial, void* ws,
+                          uint32_t wait_ns);
+// the bound of the mbarrier waits in the tensor-memory and TMA kernels (ns; 0: default)
+uint32_t wait_limit_ns();
 // weighted sum of split partials (o[256], m, l rows of 260 floats) -> out, launched programmatically dependent
 int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out);
+// the splits of a one-query decode merged into one unnormalised partial row per (sequence, query head)
+int launch_combine_partial(const Launch& L, const float* ws, int splits, int n_seqs, int H, float* partial);
+// gathered partials [n_parts][n_seqs][rows][260] -> out [n_seqs][rows][256]
+int launch_combine_parts(const Launch& L, const float* parts, int n_parts, int n_seqs, int n_rows_per_seq,
+                         float* out);
 int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,
                    int seq_len, int n_q_tok, const int32_t* steps, float sm_scale, float* out);
 

@@ -97,6 +97,7 @@ struct DecodeParams {
   int64_t max_pages;
   const int32_t* steps;
   int max_seq_len, cells_per_split, splits;
+  int cell_base, cell_limit;  // the cell range the splits cover: [cell_base, cell_limit)
   float sm_scale_log2;
   float* ws;
   int* status;
@@ -169,11 +170,12 @@ __device__ __forceinline__ float pow2i(int e) { return e < -126 ? 0.0f : __int_a
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+// one non-blocking test of the phase
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
       : "r"(bar), "r"(parity)
@@ -204,6 +206,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // that do the work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit_ns, const volatile int* abort) {
   if (mbar_try(bar, parity)) return true;
+  if (limit_ns < 1000u) return false;        // a bound under 1 us: one poll, no waiting
   const uint64_t t0 = global_ns();
   for (;;) {
     if (global_ns() - t0 >= limit_ns) return false;
@@ -314,8 +317,8 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
     if (threadIdx.x == 0 && split == 0 && g == 0) record_status(p.status, K8V4_ERANGE);
     n_vis = n_vis < 0 ? 0 : p.max_seq_len;
   }
-  const int c_begin = split * p.cells_per_split;
-  const int c_stop = c_begin + p.cells_per_split;
+  const int c_begin = p.cell_base + split * p.cells_per_split;
+  const int c_stop = min(c_begin + p.cells_per_split, p.cell_limit);
   const int c_end = min(c_stop, n_vis);
   const int n_tiles = c_end > c_begin ? (c_end - c_begin + 15) >> 4 : 0;
   const int n_my = n_tiles > w ? (n_tiles - w + W - 1) / W : 0;      // tiles w + W u
@@ -542,16 +545,19 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
       sc[3] = vB ? (kB.x * (acc[0][3] + acc[1][3]) + kB.y * (acc[2][3] + acc[3][3])) * f1 : -INFINITY;
 
       // ---- softmax: the running bucket per head, raised by this tile's
-      // ceil(max / 8); the accumulators follow by an exact power of two
-      float t0 = fmaxf(sc[0], sc[2]), t1 = fmaxf(sc[1], sc[3]);
+      // ceil(max / 8); the accumulators follow by an exact power of two.  No
+      // score above the running reference 8 M needs no maximum at all.
+      int nb0 = M0, nb1 = M1;
+      const bool up0 = sc[0] > 8.0f * M0 || sc[2] > 8.0f * M0, up1 = sc[1] > 8.0f * M1 || sc[3] > 8.0f * M1;
+      if (__any_sync(kFull, up0 || up1)) {
+        float t0 = fmaxf(sc[0], sc[2]), t1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, off));
-        t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, off));
-      }
-      const int nb0 = max(M0, static_cast<int>(fminf(fmaxf(ceilf(t0 * 0.125f), -kBucketClamp), kBucketClamp)));
-      const int nb1 = max(M1, static_cast<int>(fminf(fmaxf(ceilf(t1 * 0.125f), -kBucketClamp), kBucketClamp)));
-      if (__any_sync(kFull, nb0 != M0 || nb1 != M1)) {
+        for (int off = 4; off < 32; off <<= 1) {
+          t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, off));
+          t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, off));
+        }
+        nb0 = max(M0, static_cast<int>(fminf(fmaxf(ceilf(t0 * 0.125f), -kBucketClamp), kBucketClamp)));
+        nb1 = max(M1, static_cast<int>(fminf(fmaxf(ceilf(t1 * 0.125f), -kBucketClamp), kBucketClamp)));
         const float g0 = M0 == INT_MIN ? 0.0f : pow2i(8 * (M0 - nb0));
         const float g1 = M1 == INT_MIN ? 0.0f : pow2i(8 * (M1 - nb1));
 #pragma unroll
@@ -824,7 +830,7 @@ bool maps_of(const CacheView& C, CUtensorMap* k, CUtensorMap* v) {
 }
 
 template <int FMT, bool QF32>
-int launch_impl(const Launch& L, DecodeParams p, int n_seqs, float* out) {
+int launch_impl(const Launch& L, DecodeParams p, int n_seqs, float* out, bool partial) {
   p.L = layout_of(FMT, p.C.H, QF32 ? kMaxWorkersF32 : kMaxWorkers);
   CUtensorMap mk, mv;
   if (!maps_of(p.C, &mk, &mv)) return K8V4_ECUDA;
@@ -845,7 +851,8 @@ int launch_impl(const Launch& L, DecodeParams p, int n_seqs, float* out) {
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kern, mk, mv, p) != cudaSuccess) return K8V4_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
-  return launch_combine(L, p.ws, p.splits, n_seqs, 1, p.C.H, out);
+  return partial ? launch_combine_partial(L, p.ws, p.splits, n_seqs, p.C.H, out)
+                 : launch_combine(L, p.ws, p.splits, n_seqs, 1, p.C.H, out);
 }
 
 }  // namespace
@@ -883,11 +890,10 @@ AttendPlan plan_decode(const CacheView& C, int n_seqs, int max_seq_len, int num_
   return pl;
 }
 
-int launch_decode(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
-                  const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
-                  float sm_scale, float* out, void* ws, const void* k_new, const void* v_new, int kv_dtype,
-                  uint32_t wait_ns) {
-  if (n_seqs == 0) return K8V4_OK;
+namespace {
+DecodeParams params_of(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, const int32_t* pt,
+                       int64_t max_pages, const int32_t* steps, int max_seq_len, float sm_scale, void* ws,
+                       uint32_t wait_ns) {
   DecodeParams p;
   p.C = C;
   p.q = q;
@@ -897,20 +903,48 @@ int launch_decode(const Launch& L, const CacheView& C, const AttendPlan& plan, c
   p.max_seq_len = max_seq_len;
   p.cells_per_split = plan.cells_per_split;
   p.splits = plan.splits;
+  p.cell_base = 0;
+  p.cell_limit = max_seq_len;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.ws = static_cast<float*>(ws);
   p.status = L.status;
+  p.k_new = nullptr;
+  p.v_new = nullptr;
+  p.kv_bf16 = 1;
+  p.wait_ns = wait_ns ? wait_ns : kWaitDefaultNs;
+  p.page_div = FastDiv(static_cast<uint32_t>(C.P));
+  return p;
+}
+int dispatch(const Launch& L, const DecodeParams& p, int fmt, bool f32, int n_seqs, float* out, bool partial) {
+  if (fmt == K8V4_FORMAT_K8V4)
+    return f32 ? launch_impl<K8V4_FORMAT_K8V4, true>(L, p, n_seqs, out, partial)
+               : launch_impl<K8V4_FORMAT_K8V4, false>(L, p, n_seqs, out, partial);
+  return f32 ? launch_impl<K8V4_FORMAT_INT8, true>(L, p, n_seqs, out, partial)
+             : launch_impl<K8V4_FORMAT_INT8, false>(L, p, n_seqs, out, partial);
+}
+}  // namespace
+
+int launch_decode(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
+                  const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
+                  float sm_scale, float* out, void* ws, const void* k_new, const void* v_new, int kv_dtype,
+                  uint32_t wait_ns) {
+  if (n_seqs == 0) return K8V4_OK;
+  DecodeParams p = params_of(L, C, plan, q, pt, max_pages, steps, max_seq_len, sm_scale, ws, wait_ns);
   p.k_new = k_new;
   p.v_new = v_new;
   p.kv_bf16 = kv_dtype == K8V4_BF16 ? 1 : 0;
-  p.wait_ns = wait_ns ? wait_ns : kWaitDefaultNs;
-  p.page_div = FastDiv(static_cast<uint32_t>(C.P));
-  const bool f32 = q_dtype == K8V4_F32;
-  if (C.fmt == K8V4_FORMAT_K8V4)
-    return f32 ? launch_impl<K8V4_FORMAT_K8V4, true>(L, p, n_seqs, out)
-               : launch_impl<K8V4_FORMAT_K8V4, false>(L, p, n_seqs, out);
-  return f32 ? launch_impl<K8V4_FORMAT_INT8, true>(L, p, n_seqs, out)
-             : launch_impl<K8V4_FORMAT_INT8, false>(L, p, n_seqs, out);
+  return dispatch(L, p, C.fmt, q_dtype == K8V4_F32, n_seqs, out, false);
+}
+
+int launch_decode_partial(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
+                          const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs,
+                          int max_seq_len, int cell_begin, int cell_end, float sm_scale, float* partial, void* ws,
+                          uint32_t wait_ns) {
+  if (n_seqs == 0) return K8V4_OK;
+  DecodeParams p = params_of(L, C, plan, q, pt, max_pages, steps, max_seq_len, sm_scale, ws, wait_ns);
+  p.cell_base = cell_begin;
+  p.cell_limit = cell_end;
+  return dispatch(L, p, C.fmt, q_dtype == K8V4_F32, n_seqs, partial, true);
 }
 
 }  // namespace k8v4

@@ -73,7 +73,7 @@ static_assert(kBarOff - kKfOff >= 128 * 256 * 4, "epilogue buffer");
 constexpr uint32_t kTmemCols = 512;    // S buffers [0,128) and [128,256) (S0 | S1 each; P1/P2 reuse
                                        // the buffer's S0 columns), O_tile [256,512)
 constexpr uint32_t kSBuf = 128, kS0Col = 0, kS1Col = 64, kOCol = 256, kP1Col = 0, kP2Col = 32;
-constexpr uint32_t kSpinLimit = 1u << 22;     // ~1 s of try_wait polling
+constexpr uint32_t kWaitDefaultNs = 1000000000u;   // 1 s: the default bound of an mbarrier wait
 constexpr float kSlack = 8.0f;                // log2 headroom of P above its row's reference maximum
 constexpr int kChain = 4;                     // tiles accumulated in one TMEM O tile at most
 
@@ -89,26 +89,52 @@ struct PrefillParams {
   float* out;              // final rows [n_seqs][n_q_tok][HQ][256], or null
   float* ws;               // else partial rows (o[256], m, l) for the combine
   int* status;
+  uint32_t wait_ns;        // bound of the pipeline's mbarrier waits, nanoseconds
 };
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-// Wait for the phase with parity `parity` to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity, uint32_t sleep_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(sleep_ns)
+      : "memory");
+  return done != 0;
+}
+// one non-blocking test of the phase
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase with parity `parity` to complete; false once `limit_ns`
+// nanoseconds have passed without it.  The waiting thread sleeps in the barrier
+// (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  if (limit_ns < 1000u) return false;        // a bound under 1 us: one poll, no waiting
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (global_ns() - t0 >= limit_ns) return false;
+    if (mbar_try(bar, parity, 20000u)) return true;
   }
-  return false;
 }
 // 2^x on the special-function unit (approximate, subnormal results flushed to 0)
 __device__ __forceinline__ float ex2_ftz(float x) {
@@ -489,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 
   // wait on `bar` (warp 0 polls) and OR `pred` over the CTA: 1 / 0, or -1 on timeout
   auto wait_bar_or = [&](uint32_t bar, uint32_t& phase, bool pred) -> int {
-    if (warp == 0 && !mbar_wait(bar, phase & 1) && lane == 0) *reinterpret_cast<volatile int*>(flag_s) = 1;
+    if (warp == 0 && !mbar_wait(bar, phase & 1, p.wait_ns) && lane == 0) *reinterpret_cast<volatile int*>(flag_s) = 1;
     ++phase;
     const int any = __syncthreads_or(pred ? 1 : 0);
     if (*reinterpret_cast<volatile int*>(flag_s)) { failed = true; return -1; }
@@ -497,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     return any;
   };
   auto wait_bar = [&](uint32_t bar, uint32_t& phase) -> bool {   // one warp polls, all synchronise
-    if (warp == 0 && !mbar_wait(bar, phase & 1)) failed = true;
+    if (warp == 0 && !mbar_wait(bar, phase & 1, p.wait_ns)) failed = true;
     ++phase;
     if (__syncthreads_or(failed ? 1 : 0)) { failed = true; return false; }
     tc_fence_after();
@@ -680,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   } else {
     if (tid == 0) {
       record_status(p.status, K8V4_ECUDA);
-      mma_commit(bar_d);                     // let in-flight MMAs drain (bounded)
-      (void)mbar_wait(bar_d, 0);
+      mma_commit(bar_d);                     // let in-flight MMAs drain (bounded by the default)
+      (void)mbar_wait(bar_d, 0, kWaitDefaultNs);
     }
   }
   tc_fence_before();
@@ -714,6 +740,7 @@ int launch_prefill(const Launch& L, const CacheView& C, const void* q, const int
   p.out = out;
   p.ws = nullptr;
   p.status = L.status;
+  p.wait_ns = wait_limit_ns() ? wait_limit_ns() : kWaitDefaultNs;
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return K8V4_ECUDA;
   const dim3 grid((n_q_tok + kTokens - 1) / kTokens, C.H, 1);
@@ -763,6 +790,7 @@ int launch_verify_tc(const Launch& L, const CacheView& C, const AttendPlan& plan
   p.out = nullptr;
   p.ws = static_cast<float*>(ws);
   p.status = L.status;
+  p.wait_ns = wait_limit_ns() ? wait_limit_ns() : kWaitDefaultNs;
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return K8V4_ECUDA;
   const dim3 grid((plan.n_q + kTokens - 1) / kTokens, C.H, n_seqs * plan.splits);

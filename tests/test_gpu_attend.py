@@ -202,7 +202,7 @@ def test_verify_config4_full_sampled():
     assert rel_err(gsel, want) <= TOL
 
 
-@pytest.mark.parametrize("n_cells", [237568, 262144, 118784 + 37])
+@pytest.mark.parametrize("n_cells", [14848, 118784, 237568, 262144, 118784 + 37])
 def test_decode_long_context(n_cells):
     """Config 3 lengths (and one non-aligned length): all 16 rows against the oracle;
     the INT8 and Q4 comparison arms at the 238K point too."""

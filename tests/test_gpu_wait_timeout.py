@@ -1,0 +1,71 @@
+"""The bounded-wait failure path of the mbarrier-driven kernels, made to run on
+the GPU without a fault: with the wait bound set below 1 us every wait that is
+not already complete gives up after one poll (the barrier would still complete on its
+own), so the kernel records K8V4_ECUDA, waits (with its default bound) for its
+own copies and MMAs, releases what it holds (tensor memory for prefill) and
+returns.  A normal call in the same process afterwards must match the oracle,
+which shows the context and the tensor memory are intact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_paged_kv_q8_gb300 as k8
+import synth
+from gpu_util import TOL, append_both, decode_gpu, dev_tensor, make_caches, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _cache(seed, n_cells):
+    w = synth.decode_workload(seed, n_cells, P=64, name="timeout")
+    gpu, ref = make_caches(w.n_pages, 64, 2)
+    pt_d = append_both(gpu, ref, w.page_table, w.pos, synth.Tensor(w.k.f32[None], "bf16"),
+                       synth.Tensor(w.v.f32[None], "bf16"))
+    return w, gpu, ref, pt_d
+
+
+def test_prefill_wait_timeout_then_recovery():
+    w, gpu, ref, pt_d = _cache(synth.config_seed(5) + 901, 256)
+    n_tok = 16
+    q = synth.q_values(w.seed, 9, n_tok, 2, "bf16")
+    q_d = dev_tensor(q, (n_tok, 16, 256))
+    out = torch.empty(n_tok, 16, 256, device="cuda")
+    assert k8.k8v4_last_device_status() == 0
+    try:
+        k8.k8v4_set_wait_limit_ns(1)
+        k8.attn_k8v4_prefill(gpu, q_d, pt_d[0], 256, out)
+        assert k8.k8v4_last_device_status() == k8.ECUDA
+    finally:
+        k8.k8v4_set_wait_limit_ns(0)   # back to each kernel's default
+    k8.attn_k8v4_prefill(gpu, q_d, pt_d[0], 256, out)
+    assert k8.k8v4_last_device_status() == 0
+    steps = (256 - n_tok + 1 + np.arange(n_tok)).astype(np.int32)
+    rs, rh, rv = oracle.multi_query_rows(steps[None], 16)
+    want = ref.attention(w.page_table, rs, rh, rv, q.f32.reshape(-1, 256))
+    assert rel_err(out.cpu().numpy().reshape(-1, 256), want) <= TOL
+
+
+def test_decode_wait_timeout_then_recovery():
+    n = 32768
+    w, gpu, ref, pt_d = _cache(synth.config_seed(2) + 902, n)
+    q = synth.q_values(w.seed, 9, 1, 2, "bf16")
+    q_d = dev_tensor(q, (1, 16, 256))
+    assert k8.k8v4_last_device_status() == 0
+    # the cache must come from HBM, not L2, so that no copy can land before a
+    # warp first polls its stage: overwrite L2 with a buffer larger than it
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush.fill_(1)
+    torch.cuda.synchronize()
+    try:
+        k8.k8v4_set_wait_limit_ns(1)
+        decode_gpu(gpu, q_d, pt_d, w.seq_lens, n)
+        assert k8.k8v4_last_device_status() == k8.ECUDA
+    finally:
+        k8.k8v4_set_wait_limit_ns(0)
+    del flush
+    got = decode_gpu(gpu, q_d, pt_d, w.seq_lens, n)
+    assert k8.k8v4_last_device_status() == 0
+    rs, rh, rv = oracle.decode_rows(1, 16, w.seq_lens)
+    want = ref.attention(w.page_table, rs, rh, rv, q.f32.reshape(-1, 256))
+    assert rel_err(got.reshape(-1, 256), want) <= TOL

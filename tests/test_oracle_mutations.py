@@ -27,7 +27,7 @@ MUTATIONS = [
     ("hadamard index", "__builtin_popcount((unsigned)(i & j))", "__builtin_popcount((unsigned)(i | j))"),
     ("V run offset", "p.vq = base + 264 * H * P + r * 128;", "p.vq = base + 256 * H * P + r * 128;"),
     ("GQA map", "g = h / GQA;", "g = h % a->C.H;"),
-    ("softmax scale dropped", "sc[j] = dot * a->sm_scale;", "sc[j] = dot;"),
+    ("softmax scale dropped", "sc[j] = dot * sm_scale;", "sc[j] = dot;"),
     ("inverse rotation scale", "o[i] = s / 16.0;", "o[i] = s / 8.0;"),
     ("one cell short", "n = a->row_vis[r], g", "n = a->row_vis[r] - (a->row_vis[r] > 0), g"),
     ("q4 K left rotated", "orc_hadamard_rotate(kr, k_out + off);", "memcpy(k_out + off, kr, sizeof kr);"),

@@ -413,6 +413,47 @@ def test_attention_matches_torch_sdpa(orc, fmt):
             assert np.max(np.abs(got[h] - ref)) < 1e-12 * max(1.0, np.max(np.abs(ref)))
 
 
+def _merge_partials(parts):
+    """sum_r e^(m_r - M) o_r / sum_r e^(m_r - M) l_r over (o, m, l) triples, fp64."""
+    M = np.max(np.stack([m for _, m, _ in parts]), axis=0)
+    num = np.zeros_like(parts[0][0])
+    den = np.zeros_like(parts[0][1])
+    for o, m, l in parts:
+        w = np.where(np.isneginf(m), 0.0, np.exp(np.where(np.isneginf(m), 0.0, m - M)))
+        num += w[:, None] * o
+        den += w * l
+    return num / np.where(den > 0, den, 1.0)[:, None]
+
+
+@pytest.mark.parametrize("fmt", ["k8v4", "int8"])
+def test_attention_partial_merge_equals_full(orc, fmt):
+    """The partial attention of a cell range (the cell-range split of one decode
+    across GPUs) merges back to the full attention: for random partitions of the
+    visible cells into ranges (empty ones included), the merge of the ranges'
+    (o, m, l) equals the full fp64 attention, itself pinned to torch SDPA; a
+    single range [0, n) gives o / l = attention and l >= 1; an empty range gives
+    m = -inf, l = 0, o = 0."""
+    f = orc.FMT_K8V4 if fmt == "k8v4" else orc.FMT_INT8
+    cache, pt, n = _small_cache(orc, f, seed=21, n=93)
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((16, D)).astype(np.float32)
+    rs, rh, rv = orc.decode_rows(1, 16, [n])
+    full = cache.attention(pt, rs, rh, rv, q)
+    for trial in range(6):
+        cuts = np.sort(rng.integers(0, n + 1, size=rng.integers(1, 5)))
+        bounds = [0, *cuts.tolist(), n]
+        parts = []
+        for lo, hi in zip(bounds[:-1], bounds[1:]):
+            parts.append(cache.attention_partial(pt, rs, rh, np.full(16, lo), np.full(16, hi), q))
+        got = _merge_partials(parts)
+        assert np.max(np.abs(got - full)) < 1e-12 * max(1.0, np.max(np.abs(full)))
+    o, m, l = cache.attention_partial(pt, rs, rh, np.zeros(16), np.full(16, n), q)
+    assert np.max(np.abs(o / l[:, None] - full)) < 1e-12 * max(1.0, np.max(np.abs(full)))
+    assert np.all(l >= 1.0)
+    o, m, l = cache.attention_partial(pt, rs, rh, np.full(16, 50), np.full(16, 50), q)
+    assert np.all(np.isneginf(m)) and np.all(l == 0.0) and np.all(o == 0.0)
+
+
 def test_attention_closed_forms(orc):
     """One visible cell returns that cell's V; q = 0 returns the plain mean of the
     visible cells' V (equal scores)."""

@@ -44,6 +44,30 @@ CELL_BYTES_Q4 = 576
 APPEND_BYTES = 2 * H * 256 * 2 + CELL_BYTES      # bf16 K+V in, 816 B out
 METRIC = "k8v4 decode-attn GB/s (% HBM peak) and cells/s @238K ctx; append cells/s"
 WORKLOAD = "decode_237568_cells_2kv_16q_gqa8_P64_bf16"
+SWEEP = (14848, 118784, 237568, 262144)       # the long-context sweep (page-aligned 15K/119K/238K/262,144)
+L2_BYTES = 129 << 20
+
+
+def config_dict(world: int) -> dict:
+    """The workload both arms report (the GPU line and the reference arm)."""
+    return {"workload": WORKLOAD, "cells": N_CELLS, "page_size": P, "n_kv_heads": H, "n_q_heads": HQ,
+            "step": "append 1 token + split-K decode attention (partials + combine/inverse WHT), one call "
+                    "(attn_k8v4_decode_step: the CTA holding the newest cell writes it first)",
+            "l2": "inputs larger than L2: two 193.9 MB cache replicas alternate (387.7 MB > 135.5 MB L2)",
+            "parallelism": f"replicas x{world}"}
+
+
+def prefix_workload(big, n_cells: int):
+    """The first n_cells of a long-context workload with the page table that
+    synth.config3(n_cells) draws (the K/V/q streams are counter-based, so the
+    prefix holds config3(n_cells)'s values)."""
+    import synth
+    n_pages = (n_cells + P - 1) // P
+    pt = synth.page_table_shuffled(big.seed, synth.stream_id(synth.T_PT, 0), n_pages, n_pages)
+    return synth.Workload(name=f"decode_{n_cells}", seed=big.seed, n_seqs=1, page_size=P, n_kv=H,
+                          n_pages=n_pages, max_pages=n_pages, page_table=pt.reshape(1, -1),
+                          seq_lens=np.array([n_cells], np.int32), pos=np.array([0], np.int64),
+                          k=big.k, v=big.v, q=big.q, dtype=big.dtype)
 
 
 def dist_info():
@@ -208,14 +232,239 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "cells": N_CELLS, "sample_cells": n_cells},
+            "config": config_dict(ws), "sample_cells": n_cells,
             "cells_per_s": n_cells / dt,
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def run_oracle_table(args):
+    """The CPU oracle per configuration, on 1 thread and on every host thread
+    (the baseline plan's table): decode GB/s over 816 B/cell, verify GB/s over
+    the cells read, prefill TFLOP/s over the visible (query, cell) pairs x 16
+    heads x 1,024 flop, append cells/s.  Large cases are timed on a stated
+    sample and scaled linearly (attention cost is linear in rows)."""
+    import oracle
+    import synth
+    nt = os.cpu_count() or 1
+
+    def timed(fn, min_s=0.5):
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_s:
+                return dt / n
+
+    def decode_case(w, n_cells, label):
+        n_pages = (n_cells + P - 1) // P
+        pt = np.arange(n_pages, dtype=np.int32)[None]
+        cache = oracle.Cache(n_pages, P, H)
+        cache.append(pt, np.array([0]), w.k.f32[None, :n_cells], w.v.f32[None, :n_cells], n_threads=nt)
+        rs, rh, rv = oracle.decode_rows(1, HQ, [n_cells])
+        q = w.q.f32.reshape(-1, 256)
+        res = {"config": label, "cells": n_cells, "unit": "GB/s"}
+        for th in (1, nt):
+            dt = timed(lambda: cache.attention(pt, rs, rh, rv, q, n_threads=th))
+            res[f"t{th}"] = CELL_BYTES * n_cells / dt / 1e9
+        print(json.dumps(res), flush=True)
+
+    # config 1: the tiny fp32 round trip (append + one decode query), cells/s
+    w1 = synth.config1()
+    for th in (1, nt):
+        def rt():
+            c = oracle.Cache(w1.n_pages, w1.page_size, w1.n_kv)
+            c.append(w1.page_table, w1.pos, w1.k.f32[None], w1.v.f32[None], n_threads=th)
+            rs, rh, rv = oracle.decode_rows(1, HQ, w1.seq_lens)
+            c.attention(w1.page_table, rs, rh, rv, w1.q.f32.reshape(-1, 256), n_threads=th)
+        dt = timed(rt)
+        print(json.dumps({"config": "1 tiny round trip", "cells": 1024, "unit": "cells/s", f"t{th}": 1024 / dt}),
+              flush=True)
+    decode_case(synth.config2(), 32768, "2 decode 32,768")
+    big = synth.config3(SWEEP[-1])
+    for n in SWEEP:
+        decode_case(big, n, f"3 decode {n}")
+    # config 4: verify, 8 sequences x 5 queries; 1 thread on sequence 0 (scaled by
+    # the cells of all 8), every thread on all 8
+    w4 = synth.config4()
+    cache4 = oracle.Cache(w4.n_pages, w4.page_size, w4.n_kv)
+    for b in range(w4.n_seqs):
+        cache4.append(w4.page_table[b:b + 1], np.array([0]), w4.k[b].f32[None], w4.v[b].f32[None], n_threads=nt)
+    cells = int(w4.seq_lens.sum())
+    res = {"config": "4 verify 8 x 5", "cells": cells, "unit": "GB/s"}
+    for th, seqs in ((1, [0]), (nt, list(range(w4.n_seqs)))):
+        steps = w4.steps[seqs]
+        rs, rh, rv = oracle.multi_query_rows(steps, HQ)
+        rs = np.asarray(seqs, np.int32)[rs]
+        q = np.concatenate([w4.q[b].f32.reshape(-1, 256) for b in seqs])
+        dt = timed(lambda: cache4.attention(w4.page_table, rs, rh, rv, q, n_threads=th))
+        done = int(w4.seq_lens[seqs].sum())
+        res[f"t{th}"] = CELL_BYTES * cells / (dt * cells / done) / 1e9
+    res["sample_t1"] = "sequence 0 only, scaled by cells"
+    print(json.dumps(res), flush=True)
+    del cache4
+    # config 5: prefill of the 8,192-token chunk at 229,376 and its append; a
+    # strided query subset, scaled by the visible pairs of the whole chunk
+    w5 = synth.config5()
+    cache5 = oracle.Cache(w5.n_pages, w5.page_size, w5.n_kv)
+    hk, hv = synth.prefill_kv(w5, 0, w5.history)
+    cache5.append(w5.page_table, np.array([0]), hk.f32[None], hv.f32[None], n_threads=nt)
+    ck, cv = synth.prefill_kv(w5, w5.history, w5.chunk)
+    res = {"config": "5 chunk append 8,192", "cells": w5.chunk, "unit": "cells/s"}
+    for th in (1, nt):
+        dt = timed(lambda: cache5.append(w5.page_table, np.array([w5.history]), ck.f32[None], cv.f32[None],
+                                         n_threads=th), min_s=1.0)
+        res[f"t{th}"] = w5.chunk / dt
+    print(json.dumps(res), flush=True)
+    qall = synth.prefill_q(w5).f32.reshape(w5.chunk, HQ, 256)
+    pairs = sum(w5.history + t + 1 for t in range(w5.chunk))
+    res = {"config": "5 prefill 8,192 @ 229,376", "unit": "TFLOP/s"}
+    for th, stride in ((1, 1024), (nt, 64)):
+        toks = np.arange(0, w5.chunk, stride)
+        rs = np.zeros(len(toks) * HQ, np.int32)
+        rh = np.tile(np.arange(HQ, dtype=np.int32), len(toks))
+        rv = np.repeat((w5.history + toks + 1).astype(np.int32), HQ)
+        q = qall[toks].reshape(-1, 256)
+        dt = timed(lambda: cache5.attention(w5.page_table, rs, rh, rv, q, n_threads=th), min_s=0.1)
+        sub_pairs = int(np.sum(w5.history + toks + 1))
+        res[f"t{th}"] = pairs * HQ * 1024 / (dt * pairs / sub_pairs) / 1e12
+        res[f"sample_t{th}"] = f"every {stride}th query token ({len(toks)} tokens x 16 heads), scaled by visible pairs"
+    print(json.dumps(res), flush=True)
+    print(json.dumps({"host_threads": nt}), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
+
+def graph_ms(call, n_calls: int, reps: int) -> float:
+    """Per-call device time of `call(i)` for i < n_calls, captured once into a
+    CUDA graph and replayed `reps` times between two events (no host launch cost
+    inside the timed region)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(min(n_calls, 4)):
+            call(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for i in range(n_calls):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * n_calls)
+    del g
+    return ms
+
+
+def measure_sweep(dev, big, kd_big, vd_big, reps: int = 200):
+    """The long-context sweep: decode attention over 14,848, 118,784, 237,568 and
+    262,144 cells, the k8v4 format (816 B/cell) beside the INT8/INT8 comparison
+    format (1,056 B/cell), each timed over `reps` calls that cycle through enough
+    cache replicas to hold four times L2 (every call streams its cache from HBM):
+    once as eager calls from Python (host launch cost included) and once as a
+    CUDA graph of the same calls replayed (device time of the launches alone)."""
+    import math
+    import torch
+    import quantized_paged_kv_q8_gb300 as k8
+    hbm = peaks()[0]
+    q = torch.from_numpy(big.q.dev.view(np.int16)).view(torch.bfloat16).reshape(1, HQ, 256).to(dev)
+    zero = torch.zeros(1, dtype=torch.int64, device=dev)
+    out = torch.empty(1, HQ, 256, dtype=torch.float32, device=dev)
+    rows = []
+    for n in SWEEP:
+        w = prefix_workload(big, n)
+        pt = torch.from_numpy(w.page_table).to(dev)
+        lens = torch.full((1,), n, dtype=torch.int32, device=dev)
+        row = {"cells": n}
+        for name, fmt, cb in (("k8v4", k8.FORMAT_K8V4, CELL_BYTES), ("int8", k8.FORMAT_INT8, CELL_BYTES_INT8)):
+            n_rep = max(2, math.ceil(4 * L2_BYTES / (n * cb)))
+            caches = [k8.PagedCache(w.n_pages, P, H, fmt=fmt, device=dev) for _ in range(n_rep)]
+            for c in caches:
+                k8.kv_append_k8v4(c, pt, zero, kd_big[:, :n], vd_big[:, :n])
+            ws = k8.workspace(caches[0], 1, 1, n, device=dev)
+            for i in range(2 * n_rep):
+                k8.attn_k8v4_decode(caches[i % n_rep], q, pt, lens, n, out, ws)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(reps):
+                k8.attn_k8v4_decode(caches[i % n_rep], q, pt, lens, n, out, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            assert k8.k8v4_last_device_status() == 0
+            ms = e0.elapsed_time(e1) / reps
+            gbs = cb * n / (ms / 1e3) / 1e9
+            gms = graph_ms(lambda i: k8.attn_k8v4_decode(caches[i % n_rep], q, pt, lens, n, out, ws),
+                           n_calls=n_rep * max(1, 64 // n_rep), reps=max(2, reps // 64))
+            assert k8.k8v4_last_device_status() == 0
+            ggbs = cb * n / (gms / 1e3) / 1e9
+            row[name] = {"ms_per_step": ms, "gbs": gbs, "frac_hbm": gbs / hbm, "cells_per_s": n / (ms / 1e3),
+                         "graph": {"ms_per_step": gms, "gbs": ggbs, "frac_hbm": ggbs / hbm},
+                         "replicas": n_rep, "bytes_per_cell": cb}
+            del caches, ws
+            torch.cuda.empty_cache()
+        row["k8v4_speedup"] = row["int8"]["ms_per_step"] / row["k8v4"]["ms_per_step"]
+        row["k8v4_speedup_graph"] = row["int8"]["graph"]["ms_per_step"] / row["k8v4"]["graph"]["ms_per_step"]
+        rows.append(row)
+    return rows
+
+
+def measure_config2(dev, steps: int = 1000):
+    """Config 2: one 32,768-cell sequence (P = 64, shuffled pages, bf16), 1,000
+    decode steps (each appends the newest token and decodes, one
+    attn_k8v4_decode_step call), cycling through 21 cache replicas (561 MB, four
+    times L2).  GB/s over 816 B/cell, as eager calls and as a replayed CUDA graph
+    of 1,000 steps."""
+    import math
+    import torch
+    import quantized_paged_kv_q8_gb300 as k8
+    import synth
+    w = synth.config2()
+    n = 32768
+    pt = torch.from_numpy(w.page_table).to(dev)
+    kd = torch.from_numpy(w.k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, n, H, 256).to(dev)
+    vd = torch.from_numpy(w.v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, n, H, 256).to(dev)
+    zero = torch.zeros(1, dtype=torch.int64, device=dev)
+    n_rep = max(2, math.ceil(4 * L2_BYTES / (n * CELL_BYTES)))
+    caches = [k8.PagedCache(w.n_pages, P, H, device=dev) for _ in range(n_rep)]
+    for c in caches:
+        k8.kv_append_k8v4(c, pt, zero, kd, vd)
+    q = torch.from_numpy(w.q.dev.view(np.int16)).view(torch.bfloat16).reshape(1, HQ, 256).to(dev)
+    k_new, v_new = kd[0, n - 1:].contiguous(), vd[0, n - 1:].contiguous()
+    lens = torch.full((1,), n, dtype=torch.int32, device=dev)
+    out = torch.empty(1, HQ, 256, dtype=torch.float32, device=dev)
+    ws = k8.workspace(caches[0], 1, 1, n, device=dev)
+    for i in range(20):
+        k8.attn_k8v4_decode_step(caches[i % n_rep], q, k_new, v_new, pt, lens, n, out, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        k8.attn_k8v4_decode_step(caches[i % n_rep], q, k_new, v_new, pt, lens, n, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    ms = e0.elapsed_time(e1) / steps
+    gbs = CELL_BYTES * n / (ms / 1e3) / 1e9
+    gms = graph_ms(lambda i: k8.attn_k8v4_decode_step(caches[i % n_rep], q, k_new, v_new, pt, lens, n, out, ws),
+                   n_calls=steps, reps=3)
+    assert k8.k8v4_last_device_status() == 0
+    ggbs = CELL_BYTES * n / (gms / 1e3) / 1e9
+    return {"workload": "decode_step_32768_cells_x1000", "steps": steps, "replicas": n_rep, "ms_per_step": ms,
+            "gbs": gbs, "frac_hbm": gbs / peaks()[0], "cells_per_s": n / (ms / 1e3),
+            "graph": {"ms_per_step": gms, "gbs": ggbs, "frac_hbm": ggbs / peaks()[0], "cells_per_s": n / (gms / 1e3)}}
+
 
 def measure_verify(args, dev, reps: int = 20):
     """Config 4: 8 sequences, lengths U[16,384, 65,536], 5 queries each with steps
@@ -435,6 +684,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="k8v4", choices=["k8v4", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the CPU oracle per configuration on 1 and all host threads, then exit")
     ap.add_argument("--profile", default=None, choices=["decode", "prefill", "verify", "batched", "stream"],
                     help="lean single-kernel run for ncu (no replicas, INT8 arm, e2e or CPU baseline)")
     ap.add_argument("--chunk", type=int, default=8192, help="prefill chunk length (tokens)")
@@ -442,6 +693,9 @@ def main():
                     help="cache format of the --profile decode run")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.oracle_table:
+        run_oracle_table(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -468,11 +722,15 @@ def main():
             print(json.dumps({"profile": args.profile, **res}), flush=True)
         return
 
-    w = synth.config3(N_CELLS)
+    # one long-context workload: its 237,568-cell prefix is the headline, its
+    # prefixes the sweep (counter-based streams: the prefix is config3(n))
+    big = synth.config3(SWEEP[-1]) if not args.profile else synth.config3(N_CELLS)
+    w = prefix_workload(big, N_CELLS)
     n_pages = w.n_pages
     pt = torch.from_numpy(w.page_table).to(dev)
-    kd = torch.from_numpy(w.k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, N_CELLS, H, 256).to(dev)
-    vd = torch.from_numpy(w.v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, N_CELLS, H, 256).to(dev)
+    kd_big = torch.from_numpy(big.k.dev.view(np.int16)).view(torch.bfloat16).reshape(1, -1, H, 256).to(dev)
+    vd_big = torch.from_numpy(big.v.dev.view(np.int16)).view(torch.bfloat16).reshape(1, -1, H, 256).to(dev)
+    kd, vd = kd_big[:, :N_CELLS], vd_big[:, :N_CELLS]
     zero = torch.zeros(1, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -502,7 +760,7 @@ def main():
     wsp = k8.workspace(caches[0], 1, 1, N_CELLS, device=dev)
 
     if args.profile:
-        del kd, vd
+        del kd, vd, kd_big, vd_big
         torch.cuda.empty_cache()
 
     def step(i):
@@ -609,6 +867,10 @@ def main():
 
     del caches, kd, vd
     torch.cuda.empty_cache()
+    sweep = measure_sweep(dev, big, kd_big, vd_big)
+    del kd_big, vd_big
+    torch.cuda.empty_cache()
+    config2 = measure_config2(dev)
     verify = measure_verify(args, dev)
     batched = measure_batched_step(args, dev)
     stream = measure_stream(args, dev)
@@ -617,19 +879,15 @@ def main():
     hbm, bf16, bf16_sus, peak_kind = peaks()
     dec_bytes = CELL_BYTES * N_CELLS
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    traffic = traffic_record("attend_splitk_decode_237568")
+    traffic = traffic_record("decode_kernel_237568")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "storage": "int8 K + q4_0 V, 816 B/cell", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "cells": N_CELLS, "page_size": P, "n_kv_heads": H, "n_q_heads": HQ,
-                   "step": "append 1 token + split-K decode attention (partials + combine/inverse WHT), one call "
-                           "(attn_k8v4_decode_step: the CTA holding the newest cell writes it first)",
-                   "l2": "inputs larger than L2: two 193.9 MB cache replicas alternate (387.7 MB > 135.5 MB L2)",
-                   "parallelism": f"replicas x{world}"},
+        "config": config_dict(world),
         "cells_per_s": cells_per_s,
         "hbm_frac_of_step": value / hbm,
-        "roofline": {"bound": "hbm", "kernel": "attn_k8v4_decode (split-K partial + combine)",
+        "roofline": {"bound": "hbm", "kernel": "attn_k8v4_decode (TMA worker split-K kernel + combine)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "algorithmic_bytes_per_launch": dec_bytes,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)", "ms_per_launch": dec_ms},
@@ -640,6 +898,8 @@ def main():
         "q4_arm": {**q4_arm, "frac_hbm": q4_arm["gbs"] / hbm},
         "e2e": {"value": dec_bytes / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "sweep": sweep,
+        "config2": config2,
         "verify": {**verify, "frac_hbm": verify["gbs"] / hbm},
         "batched_step": {**batched, "frac_hbm": batched["gbs"] / hbm},
         "stream": stream,

@@ -792,7 +792,9 @@ bool encode_rows(CUtensorMap* m, const CacheView& C, int64_t run_off, int row_by
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The maps of the last few caches (encoding is host work, done once per cache)
+// The maps of the last kMapCache caches (encoding is host work, done once per
+// cache; a server cycling through more caches than that re-encodes)
+constexpr int kMapCache = 64;
 struct MapEntry {
   const uint8_t* pages = nullptr;
   int64_t n_pages = 0;
@@ -800,7 +802,7 @@ struct MapEntry {
   CUtensorMap k, v;
 };
 std::mutex g_map_mu;
-MapEntry g_maps[8];
+MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
 bool maps_of(const CacheView& C, CUtensorMap* k, CUtensorMap* v) {
@@ -823,7 +825,7 @@ bool maps_of(const CacheView& C, CUtensorMap* k, CUtensorMap* v) {
   e.P = C.P;
   e.H = C.H;
   e.fmt = C.fmt;
-  g_map_next = (g_map_next + 1) % 8;
+  g_map_next = (g_map_next + 1) % kMapCache;
   *k = e.k;
   *v = e.v;
   return true;

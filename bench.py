@@ -805,7 +805,8 @@ def main():
         if rank == 0:
             cb = caches[0].bytes_per_cell
             print(json.dumps({"profile": True, "format": args.format, "ms_per_step": ms_step, "decode_ms": dec_ms,
-                              "gbs": cb * N_CELLS / (dec_ms / 1e3) / 1e9}), flush=True)
+                              "gbs": cb * N_CELLS / (dec_ms / 1e3) / 1e9, "append_ms": append_s * 1e3,
+                              "append_frac": APPEND_BYTES * N_CELLS / append_s / 1e9 / peaks()[0]}), flush=True)
         return
 
     # ---- comparison formats on the same workload: INT8/INT8 (1,056 B/cell) and

@@ -18,6 +18,8 @@
 // (H x) / 16.  The warp computes it with an int64 fixed-point fast Walsh-Hadamard
 // transform whenever the vector's values span at most 2^54 (the common case);
 // otherwise it falls back to an exact multi-limb sum per output element.
+#include <algorithm>
+
 #include "k8v4_quant.cuh"
 
 namespace k8v4 {
@@ -78,6 +80,80 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, CacheV
   }
   if (role != 1) append_k_row<BF16, FMT>(C, base, r, k, elem, lane, stage[w], base2);
   if (role != 0) append_v_row<BF16, FMT>(C, base, r, v, elem, lane, stage[w], base2);
+}
+
+// ------------------------------------------------------------------ bulk bf16 append
+// The long appends of bf16 rows (a prompt chunk, a cache build): a persistent
+// grid of 8-warp CTAs, each warp striding over (seq, token, head) items; the
+// warp loads the next item's K and V rows (16 B per lane each) before it
+// quantises the current one, so every warp keeps 1 KB of loads in flight while
+// it computes.  The rows are quantised by the bf16 fast paths (int8 K, exact
+// rotation + q4_0 V, same bytes as append_kernel).
+template <int FMT, bool MIRROR>
+__global__ void __launch_bounds__(kWarps * 32, 4) append_bf16_kernel(
+    CacheView C, CacheView M, const int32_t* __restrict__ slot_of_page, const int32_t* __restrict__ pt,
+    int64_t max_pages, const int64_t* __restrict__ pos, int n_seqs, int n_tok, const uint16_t* __restrict__ k,
+    const uint16_t* __restrict__ v, FastDiv div_h, FastDiv div_tok, FastDiv div_p, int* status) {
+  __shared__ __align__(16) long long stage[kWarps][kRotScratch];
+  __shared__ float scale_tab[128];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  long long* ts = stage[w];
+  fill_int8_scale_table(scale_tab);
+  __syncthreads();
+  // the host keeps total below 2^31, and a cell that passes the range check is
+  // below max_pages * P <= 2^31, so the index arithmetic runs in 32 bits
+  const uint32_t total = static_cast<uint32_t>(n_seqs) * static_cast<uint32_t>(n_tok) * static_cast<uint32_t>(C.H);
+  const uint32_t stride = gridDim.x * kWarps;
+  uint32_t item = blockIdx.x * kWarps + w;
+  uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
+  if (item < total) {
+    kr = __ldcs(reinterpret_cast<const uint4*>(k + static_cast<int64_t>(item) * kD) + lane);
+    vr = __ldcs(reinterpret_cast<const uint4*>(v + static_cast<int64_t>(item) * kD) + lane);
+  }
+  for (; item < total; item += stride) {
+    const uint4 kc = kr, vc = vr;
+    const uint32_t next = item + stride;
+    if (next < total) {
+      kr = __ldcs(reinterpret_cast<const uint4*>(k + static_cast<int64_t>(next) * kD) + lane);
+      vr = __ldcs(reinterpret_cast<const uint4*>(v + static_cast<int64_t>(next) * kD) + lane);
+    }
+    const uint32_t it = div_h.div(item);
+    const int g = static_cast<int>(item - it * static_cast<uint32_t>(C.H));
+    const uint32_t b = div_tok.div(it);
+    const int t = static_cast<int>(it - b * static_cast<uint32_t>(n_tok));
+    const int64_t cell = pos[b] + t;
+    if (cell < 0 || cell >= max_pages * C.P) {
+      if (lane == 0) record_status(status, K8V4_ERANGE);
+      continue;
+    }
+    const uint32_t pidx = div_p.div(static_cast<uint32_t>(cell));
+    const int cslot = static_cast<int>(static_cast<uint32_t>(cell) - pidx * static_cast<uint32_t>(C.P));
+    const int64_t page = pt[static_cast<int64_t>(b) * max_pages + pidx];
+    const int64_t r = static_cast<int64_t>(cslot) * C.H + g;
+    uint8_t* base;
+    uint8_t* base2 = nullptr;
+    if (MIRROR) {
+      if (page < 0 || page >= M.n_pages) {
+        if (lane == 0) record_status(status, K8V4_ERANGE);
+        continue;
+      }
+      base = M.pages + page * M.page_bytes;
+      const int dslot = slot_of_page[page];
+      if (dslot >= 0 && dslot < C.n_pages) base2 = C.pages + static_cast<int64_t>(dslot) * C.page_bytes;
+      else if (dslot != -1 && lane == 0) record_status(status, K8V4_ERANGE);
+    } else {
+      if (page < 0 || page >= C.n_pages) {
+        if (lane == 0) record_status(status, K8V4_ERANGE);
+        continue;
+      }
+      base = C.pages + page * C.page_bytes;
+    }
+    if (FMT == K8V4_FORMAT_Q4) rot_q4_row_bf16(kc, lane, ts, base, base2, r * 128, C.ks_off() + r * 16);
+    else int8_row_bf16(kc, lane, scale_tab, base, base2, r * 256, C.ks_off() + r * 8);
+    if (FMT == K8V4_FORMAT_INT8) int8_row_bf16(vc, lane, scale_tab, base, base2, C.v_off() + r * 256, C.vs_off() + r * 8);
+    else rot_q4_row_bf16(vc, lane, ts, base, base2, C.v_off() + r * 128, C.vs_off() + r * 16);
+  }
 }
 
 // ------------------------------------------------------------------ dequant
@@ -166,6 +242,17 @@ void append_launch(const Launch& L, dim3 grid, dim3 block, const CacheView& C, c
                    const int32_t* pt, int64_t max_pages, const int64_t* pos, int n_seqs, int n_tok, const void* k,
                    const void* v, int split) {
   const FastDiv dh(static_cast<uint32_t>(C.H)), dt(static_cast<uint32_t>(n_tok)), dp(static_cast<uint32_t>(C.P));
+  if (BF16 && !split) {
+    // persistent: four 8-warp CTAs per SM, or fewer when the items run out
+    const int64_t items = static_cast<int64_t>(n_seqs) * n_tok * C.H;
+    const int64_t want = (items + kWarps - 1) / kWarps;
+    const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(want, static_cast<int64_t>(L.num_sms) * 4)));
+    const auto* kb = static_cast<const uint16_t*>(k);
+    const auto* vb = static_cast<const uint16_t*>(v);
+    if (M) append_bf16_kernel<FMT, true><<<pgrid, block, 0, L.stream>>>(C, *M, slot, pt, max_pages, pos, n_seqs, n_tok, kb, vb, dh, dt, dp, L.status);
+    else append_bf16_kernel<FMT, false><<<pgrid, block, 0, L.stream>>>(C, C, nullptr, pt, max_pages, pos, n_seqs, n_tok, kb, vb, dh, dt, dp, L.status);
+    return;
+  }
   if (M) append_kernel<BF16, FMT, true><<<grid, block, 0, L.stream>>>(C, *M, slot, pt, max_pages, pos, n_seqs, n_tok, k, v, split, dh, dt, dp, L.status);
   else append_kernel<BF16, FMT, false><<<grid, block, 0, L.stream>>>(C, C, nullptr, pt, max_pages, pos, n_seqs, n_tok, k, v, split, dh, dt, dp, L.status);
 }

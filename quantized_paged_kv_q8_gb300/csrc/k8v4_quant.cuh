@@ -365,5 +365,284 @@ __device__ __forceinline__ void append_v_row(const CacheView& C, uint8_t* base, 
   }
 }
 
+
+// ------------------------------------------------------------------ bf16 rows, fast paths
+// The bulk append of bf16 K/V rows.  Same bytes as the routines above (the
+// pull request's "What" and "How": int8 K with IEEE quotients, V rotated
+// exactly and quantised to q4_0), with fewer instructions for the common row:
+//
+//  * quotients: q = x * rcp with rcp = rcp.approx(s) (at most 1 ulp off 1/s)
+//    lies within 3.1e-5 of RN(x / s) for |x / s| <= 127.5, so rint(q) equals
+//    rint(RN(x / s)) unless q is within 1e-4 of a half-integer; such values
+//    (about 1 in 5,000) are redone with the IEEE division.  rint is taken by
+//    adding 1.5 * 2^23 (whose ulp is 1), which leaves the integer in the low
+//    mantissa bits;
+//  * rotation: a bf16 value is m * 2^(E - 134) with m < 2^8 (E its exponent
+//    field), so every element of a row is an integer multiple of 2^lo, lo =
+//    Emin - 134 (Emin: the smallest element's exponent field).  No partial sum
+//    of the 256-point transform exceeds the row's L1 norm; when that norm is at
+//    most 2^30 units of 2^lo the transform runs exactly in int32 on the integers
+//    x / 2^lo, and y = RN(s * 2^(lo - 4)) is the int32 -> fp32 conversion scaled
+//    by a power of two (exact: the result is normal).  Other rows (exact zeros,
+//    subnormals, a norm too large for the smallest element's grain, inf/NaN)
+//    take the int64/multi-limb rotation above.
+
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// 8 bf16 (element 8 * lane + r: word k holds r = 2k low, 2k + 1 high) -> fp32
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 raw, float x[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+// the low bytes of four words, packed little-endian
+__device__ __forceinline__ uint32_t low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+}
+
+constexpr float kRintMagic = 12582912.0f;        // 1.5 * 2^23
+constexpr float kQuotientSlack = 0.4999f;         // |q - rint(q)| above this: redo with the IEEE quotient
+
+// The general quantisers on a bf16 row, out of line (rare rows; keeps the fast
+// loop small in the instruction cache)
+__device__ __noinline__ void int8_row_general(const uint4 raw, int lane, uint8_t* a, uint8_t* b, int64_t code_off,
+                                              int64_t scale_off) {
+  float x[8];
+  bf16x8_to_f32(raw, x);
+  uint2 kc;
+  const float s = quant_int8_half(x, kc);
+  const float s_hi = __shfl_xor_sync(kQFull, s, 16);
+  st2(a, b, code_off + 8 * lane, kc);
+  if (lane == 0) st2(a, b, scale_off, make_float2(s, s_hi));
+}
+__device__ __noinline__ void rot_q4_row_general(const uint4 raw, int lane, long long* ts, uint8_t* a, uint8_t* b,
+                                                int64_t q_off, int64_t s_off) {
+  float x[8];
+  bf16x8_to_f32(raw, x);
+  __syncwarp();
+  rotate_exact(x, lane, ts);
+  quant_q4_store(x, lane, a, b, q_off, s_off);
+  __syncwarp();
+}
+
+// RN(M / 127) for the 128 significands M = 128..255 of a bf16 value, the int8
+// scale s = RN(amax / 127) of amax = M * 2^(E - 134) being that entry scaled by
+// 2^(E - 134) (exact while s is normal).  Filled once per CTA.
+__device__ __forceinline__ void fill_int8_scale_table(float* tab) {
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = __fdiv_rn(static_cast<float>(128 + i), 127.0f);
+}
+
+// int8 of a bf16 row (two 128-element halves, lanes 0-15 and 16-31): codes at
+// code_off + 8 * lane, the two fp32 scales at scale_off
+__device__ __forceinline__ void int8_row_bf16(const uint4 raw, int lane, const float* tab, uint8_t* a, uint8_t* b,
+                                              int64_t code_off, int64_t scale_off) {
+  uint32_t m = vmax_u16x2(vmax_u16x2(raw.x & 0x7fff7fffu, raw.y & 0x7fff7fffu),
+                          vmax_u16x2(raw.z & 0x7fff7fffu, raw.w & 0x7fff7fffu));
+  m = vmax_u16x2(m, prmt(m, 0u, 0x1032u));
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) m = vmax_u16x2(m, __shfl_xor_sync(kQFull, m, o));
+  const uint32_t a16 = m & 0xffffu;                  // |largest| of this half, bf16 bits
+  const uint32_t e16 = a16 >> 7;                     // its exponent field
+  // s normal and at least 2^-125 needs E >= 10; a zero half gives s = 0
+  if (__any_sync(kQFull, a16 >= 0x7f80u || (a16 != 0u && e16 < 10u))) {
+    int8_row_general(raw, lane, a, b, code_off, scale_off);
+    return;
+  }
+  const float s = a16 == 0u ? 0.0f
+                            : __uint_as_float(__float_as_uint(tab[a16 & 0x7fu]) + ((e16 - 134u + 0u) << 23));
+  float x[8];
+  bf16x8_to_f32(raw, x);
+  const float rcp = s != 0.0f ? rcp_approx(s) : 0.0f;
+  uint32_t t[8];
+  float worst = 0.0f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const float q = __fmul_rn(x[r], rcp);
+    const float tf = __fadd_rn(q, kRintMagic);
+    worst = fmaxf(worst, fabsf(__fsub_rn(q, __fsub_rn(tf, kRintMagic))));
+    t[r] = __float_as_uint(tf);
+  }
+  if (__any_sync(kQFull, worst > kQuotientSlack)) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float q = __fmul_rn(x[r], rcp);
+      if (fabsf(__fsub_rn(q, __fsub_rn(__uint_as_float(t[r]), kRintMagic))) > kQuotientSlack)
+        t[r] = __float_as_uint(__fadd_rn(rintf(__fdiv_rn(x[r], s)), kRintMagic));
+    }
+  }
+  // |code| <= 127: the low byte of the biased word is the two's-complement code
+  st2(a, b, code_off + 8 * lane, make_uint2(low_bytes(t[0], t[1], t[2], t[3]), low_bytes(t[4], t[5], t[6], t[7])));
+  const float s_hi = __shfl_xor_sync(kQFull, s, 16);
+  if (lane == 0) st2(a, b, scale_off, make_float2(s, s_hi));
+}
+
+// Shared-memory word of transform index i for the int32 re-dealing: i with bits
+// 2-4 flipped when bit 5 is set.  All three access patterns below (two 16-byte
+// stores per lane of i = 8 lane + r; eight 4-byte accesses of layout B; two
+// 16-byte loads of layout D) then touch every bank once per wavefront.
+__device__ __forceinline__ int rot_word(int i) { return i ^ (((i >> 5) & 1) * 28); }
+
+// Rotation + q4_0 of a bf16 row: nibbles at q_off (16 B per 32-element block),
+// fp16 scales at s_off.  ts: this warp's 16-byte aligned scratch of kRotScratch
+// int64 (256 words for the int32 path; the general path needs all of it).
+__device__ __forceinline__ void rot_q4_row_bf16(const uint4 raw, int lane, long long* ts64, uint8_t* a, uint8_t* b,
+                                                int64_t q_off, int64_t s_off) {
+  int* ts = reinterpret_cast<int*>(ts64);
+  // the row's smallest magnitude (bf16 bits) and its L1 norm
+  const uint32_t w0 = raw.x & 0x7fff7fffu, w1 = raw.y & 0x7fff7fffu, w2 = raw.z & 0x7fff7fffu,
+                 w3 = raw.w & 0x7fff7fffu;
+  uint32_t mn = vmin_u16x2(vmin_u16x2(w0, w1), vmin_u16x2(w2, w3));
+  mn = vmin_u16x2(mn, prmt(mn, 0u, 0x1032u));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mn = vmin_u16x2(mn, __shfl_xor_sync(kQFull, mn, o));
+  float x[8];
+  bf16x8_to_f32(raw, x);
+  float l1 = (fabsf(x[0]) + fabsf(x[1])) + (fabsf(x[2]) + fabsf(x[3])) +
+             ((fabsf(x[4]) + fabsf(x[5])) + (fabsf(x[6]) + fabsf(x[7])));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) l1 += __shfl_xor_sync(kQFull, l1, o);   // same sum in every lane
+  // lo = emin - 134: the last bit of the smallest element, hence of every element.
+  // Every partial sum of the transform is at most the L1 norm: with the float
+  // norm (relative error < 2^-16) at most 2^30 units of 2^lo, they all stay
+  // below 2^31.  emin >= 12 keeps 2^(lo - 4) normal; inf/NaN fail the test.
+  const int emin = static_cast<int>((mn & 0xffffu) >> 7);
+  const float to_fixed = __uint_as_float(static_cast<uint32_t>(max(261 - emin, 1)) << 23);   // 2^-lo
+  if (!__all_sync(kQFull, emin >= 12 && emin <= 200 && __fmul_rn(l1, to_fixed) <= 0x1p30f)) {
+    rot_q4_row_general(raw, lane, ts64, a, b, q_off, s_off);
+    return;
+  }
+  int v[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = __float2int_rn(__fmul_rn(x[r], to_fixed));   // exact integers
+  auto stages = [&](int first, int last) {    // butterflies over register bits first..last-1
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+      if (h < first || h >= last) continue;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r & h) continue;
+        const int p = v[r], q = v[r + h];
+        v[r] = p + q;
+        v[r + h] = p - q;
+      }
+    }
+  };
+  // layout A: i = 8 lane + r -> index bits 0, 1, 2
+  stages(1, 8);
+  __syncwarp();
+  {
+    const int i0 = 8 * lane;
+    *reinterpret_cast<int4*>(ts + rot_word(i0)) = make_int4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<int4*>(ts + rot_word(i0 + 4)) = make_int4(v[4], v[5], v[6], v[7]);
+  }
+  __syncwarp();
+  // layout B: i = (lane & 7) | (r & 1) << 3 | (lane >> 3) << 4 | (r >> 1) << 6 -> bits 3, 6, 7.
+  // The word is rot_word(ib) with bit 3 toggled for odd r, plus 64 (r >> 1).
+  const int wb0 = rot_word((lane & 7) | ((lane >> 3) << 4)), wb1 = wb0 ^ 8;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = ts[((r & 1) ? wb1 : wb0) + 64 * (r >> 1)];
+  stages(1, 8);
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 8; ++r) ts[((r & 1) ? wb1 : wb0) + 64 * (r >> 1)] = v[r];
+  __syncwarp();
+  // layout D (the q4_0 layout): i = 32 (lane >> 2) + 4 (lane & 3) + (r & 3) + 16 (r >> 2):
+  // lanes 4b..4b+3 hold block b, byte j of its nibble run pairs r = j & 3 with r + 4
+  {
+    const int id = 32 * (lane >> 2) + 4 * (lane & 3);
+    const int4 lo4 = *reinterpret_cast<const int4*>(ts + rot_word(id));
+    const int4 hi4 = *reinterpret_cast<const int4*>(ts + rot_word(id + 16));
+    v[0] = lo4.x; v[1] = lo4.y; v[2] = lo4.z; v[3] = lo4.w;
+    v[4] = hi4.x; v[5] = hi4.y; v[6] = hi4.z; v[7] = hi4.w;
+  }
+  stages(4, 8);                               // index bit 4
+  {
+    const int sgn = (lane & 4) ? -1 : 1;      // index bit 5 = lane bit 2
+#pragma unroll
+    for (int r = 0; r < 8; ++r) v[r] = __shfl_xor_sync(kQFull, v[r], 4) + sgn * v[r];
+  }
+  // z = RN(s): y = z * 2^(lo - 4) exactly, so the block maximum and the codes can
+  // work on z, with the reciprocal of d carrying the 2^(lo - 4)
+  float z[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) z[r] = __int2float_rn(v[r]);
+  const float from_fixed = __uint_as_float(static_cast<uint32_t>(emin - 11) << 23);  // 2^(lo - 4)
+  // block maximum by magnitude, sign kept; an exact +/- tie goes to the lower index
+  float pmax = z[0], nmin = z[0];
+#pragma unroll
+  for (int r = 1; r < 8; ++r) {
+    pmax = fmaxf(pmax, z[r]);
+    nmin = fminf(nmin, z[r]);
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    pmax = fmaxf(pmax, __shfl_xor_sync(kQFull, pmax, o));
+    nmin = fminf(nmin, __shfl_xor_sync(kQFull, nmin, o));
+  }
+  const float ap = fabsf(pmax), an = fabsf(nmin);
+  float mz = ap > an ? pmax : (an > ap ? nmin : pmax);
+  const bool tie = ap == an && pmax != nmin;
+  if (__any_sync(kQFull, tie)) {
+    // first index (within the block) holding the magnitude ap, and its sign
+    uint32_t best = 0xffffffffu;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const uint32_t j = static_cast<uint32_t>(4 * (lane & 3) + (r & 3) + 16 * (r >> 2));
+      const uint32_t k = (j << 1) | (__float_as_uint(z[r]) >> 31);
+      if (fabsf(z[r]) == ap && k < best) best = k;
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) best = min(best, __shfl_xor_sync(kQFull, best, o));
+    if (tie) mz = (best & 1u) ? -ap : ap;
+  }
+  const __half dh = __float2half_rn(__fmul_rn(__fmul_rn(mz, from_fixed), -0.125f));
+  const float d = __half2float(dh);
+  // q = RN(y / d) ~ z * (2^(lo - 4) / d); d = +-inf gives 0, codes 8 as for y / d = 0
+  const float rcp = d != 0.0f ? __fmul_rn(rcp_approx(d), from_fixed) : 0.0f;
+  constexpr float kMagic8 = kRintMagic + 8.0f;
+  uint32_t t[8];
+  float worst = 0.0f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const float q = __fmul_rn(z[r], rcp);
+    const float tf = __fadd_rn(q, kMagic8);
+    worst = fmaxf(worst, fabsf(__fsub_rn(q, __fsub_rn(tf, kMagic8))));
+    t[r] = __float_as_uint(fminf(tf, kRintMagic + 15.0f));
+  }
+  // |y / d| <= 8 (1 + 2^-11) for a normal d: codes >= 0.  A subnormal d (or a
+  // quotient near a half-integer) takes the exact quotient and both clamps.
+  if (__any_sync(kQFull, worst > kQuotientSlack || fabsf(d) < 0x1p-14f)) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float q = __fmul_rn(z[r], rcp);
+      const float tf = __fadd_rn(q, kMagic8);
+      float c = tf;
+      if (fabsf(__fsub_rn(q, __fsub_rn(tf, kMagic8))) > kQuotientSlack)
+        c = __fadd_rn(rintf(__fdiv_rn(__fmul_rn(z[r], from_fixed), d)), kMagic8);
+      t[r] = __float_as_uint(fminf(fmaxf(c, kRintMagic), kRintMagic + 15.0f));
+    }
+  }
+  // code = low nibble of the biased word (2^22 + 8 + rint); byte j = code(r) | code(r + 4) << 4
+  const uint32_t lo = low_bytes(t[0], t[1], t[2], t[3]), hi = low_bytes(t[4], t[5], t[6], t[7]);
+  st2(a, b, q_off + 4 * lane, (lo & 0x0f0f0f0fu) | ((hi << 4) & 0xf0f0f0f0u));
+  if ((lane & 3) == 0) st2(a, b, s_off + 2 * (lane >> 2), dh);
+}
+
 }  // namespace
 }  // namespace k8v4

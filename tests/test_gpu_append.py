@@ -169,3 +169,102 @@ def test_append_rotation_fixed_point_edges(fmt):
     torch.cuda.synchronize()
     assert k8.k8v4_last_device_status() == 0
     _assert_bytes_equal(gpu, ref)
+
+
+def _sylvester():
+    i = np.arange(256)
+    return np.where(np.vectorize(lambda a: bin(a).count("1") & 1)(i[:, None] & i[None, :]), -1.0, 1.0)
+
+
+def _from_rotated(y: np.ndarray) -> np.ndarray:
+    """The row x whose exact rotation H x / 16 is y (H H = 256 I); x must be
+    exactly representable in bf16."""
+    x = _sylvester() @ np.asarray(y, np.float64) / 16.0
+    xb = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(x.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(xb, x), "crafted row is not exact in bf16"
+    return x.astype(np.float32)
+
+
+def _rotation_edge_rows(rng) -> list[np.ndarray]:
+    """bf16 rows at the edges of the append's int32 rotation path and of its
+    q4_0 quantiser: L1 norms just inside and just outside 2^30 units of the
+    smallest element's last bit, wide exponent spans, the smallest admitted
+    exponent and its neighbour, huge values, exact zeros, subnormals, +/- ties
+    for a block's largest magnitude in either order, fp16 scales that are
+    subnormal (codes clamped at 0 and 15), zero or infinite, and quotients
+    exactly halfway between codes."""
+    rows = []
+    mant = lambda n: (rng.integers(128, 256, n) / 128.0) * rng.choice([-1.0, 1.0], n)
+    for big in (32.0, 32.25):                            # L1 * 2^17 = 1.0696e9 / 1.0779e9 vs 2^30
+        r = np.full(256, big); r[1::2] *= -1; r[200] = 2.0 ** -10
+        rows.append(r)
+    for e in (-115, -116):                                # smallest element's exponent field 12 / 11
+        r = mant(256) * 2.0 ** (e + rng.integers(0, 8, 256))
+        r[17] = 2.0 ** e
+        rows.append(r)
+    mant = lambda n: (rng.integers(128, 256, n) / 128.0) * rng.choice([-1.0, 1.0], n)
+    for span in (14, 15):
+        r = mant(256) * 2.0 ** rng.integers(-4, 3, 256)
+        r[0] = 255 / 128 * 8.0
+        r[1] = -255 / 128 * 2.0 ** (3 - span)
+        rows.append(r)
+    for e in (-101, -102, 73, 74, 75, 80):               # huge and tiny rows; 80: smallest field 202
+        r = mant(256) * 2.0 ** (e - rng.integers(0, 6, 256))
+        r[9] = 1.5 * 2.0 ** e
+        rows.append(r)
+    r = mant(256); r[77] = 0.0; rows.append(r)           # one exact zero
+    r = mant(256); r[3] = 2.0 ** -130; rows.append(r)    # one subnormal
+    rows.append(np.zeros(256))
+    rows.append(mant(256) * 2.0 ** -126)                 # all at the smallest normal binade
+    # rotated-domain rows: y sparse, x = H y / 16 exact and without zeros
+    for j1, j2 in ((3, 20), (20, 3), (17, 2), (0, 31)):
+        y = np.zeros(256); y[j1] = 1.0; y[j2] = -1.0; y[200] = 4.0
+        rows.append(_from_rotated(y))
+    # block 1's largest is 11 u: its fp16 scale -11 u / 8 is subnormal and rounds to
+    # -u (codes -11 + 8 and 10 + 8 clamp to 0 and 15), flushes to zero, or overflows;
+    # every signed sum of 11, 10, 3, 1 is odd, so x has no zeros
+    for u in (2.0 ** -24, 2.0 ** -30, 2.0 ** 17):
+        y = np.zeros(256); y[40] = 11 * u; y[41] = -10 * u; y[42] = 3 * u; y[230] = u
+        rows.append(_from_rotated(y))
+    y = np.zeros(256); y[64:68] = (-8.0, 2.5, 3.5, -1.5); y[100] = 0.25; y[101] = 0.5
+    rows.append(_from_rotated(y))                        # q = y / 1 exactly k + 1/2
+    return [np.asarray(r, np.float32) for r in rows]
+
+
+def _int8_edge_rows(rng) -> list[np.ndarray]:
+    """bf16 rows at the edges of the int8 quantiser's fast path: quotients that
+    are exact half-integers (scale 1), a zero half, a tiny scale below 2^-125
+    (the general quantiser), and halves whose largest magnitude sits in either
+    lane group."""
+    rows = []
+    r = np.zeros(256); r[0] = 127.0; r[1:6] = (2.5, -3.5, 0.5, -0.5, 126.5); r[128] = -127.0; r[129:131] = (1.5, -2.5)
+    rows.append(r)
+    r = rng.standard_normal(256); r[:128] = 0.0; rows.append(r)
+    r = rng.standard_normal(256) * 2.0 ** -120; rows.append(r)
+    r = rng.standard_normal(256); r[127] = 40.0; r[255] = -40.0; rows.append(r)
+    return [synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(np.asarray(r, np.float32))) for r in rows]
+
+
+@pytest.mark.parametrize("fmt", [k8.FORMAT_K8V4, k8.FORMAT_INT8, k8.FORMAT_Q4])
+def test_append_bf16_fast_path_edges(fmt):
+    """A long bf16 append (the persistent bulk kernel) whose rows include every
+    edge of its int32 rotation and rounding shortcuts: bytes equal the oracle's
+    (rows that leave a shortcut take the general exact path)."""
+    rng = np.random.default_rng(2024)
+    n, P = 1024, 16
+    k = rng.standard_normal((1, n, 2, 256)).astype(np.float32)
+    v = rng.standard_normal((1, n, 2, 256)).astype(np.float32)
+    rot, i8 = _rotation_edge_rows(rng), _int8_edge_rows(rng)
+    rot_dst, i8_dst = (k if fmt == k8.FORMAT_Q4 else v), (v if fmt == k8.FORMAT_INT8 else k)
+    for i, r in enumerate(rot):
+        rot_dst[0, 100 + 7 * i, i % 2] = r
+        if fmt == k8.FORMAT_K8V4:
+            v[0, 600 + 5 * i, (i + 1) % 2] = -r
+    for i, r in enumerate(i8):
+        i8_dst[0, 300 + 11 * i, i % 2] = r
+    pt = np.random.default_rng(8).permutation(n // P)[None].astype(np.int32)
+    gpu, ref = make_caches(n // P, P, 2, fmt)
+    append_both(gpu, ref, pt, np.array([0]), synth.Tensor(k, "bf16"), synth.Tensor(v, "bf16"))
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    _assert_bytes_equal(gpu, ref)

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, CacheV
 // it computes.  The rows are quantised by the bf16 fast paths (int8 K, exact
 // rotation + q4_0 V, same bytes as append_kernel).
 template <int FMT, bool MIRROR>
-__global__ void __launch_bounds__(kWarps * 32, 4) append_bf16_kernel(
+__global__ void __launch_bounds__(kWarps * 32, 3) append_bf16_kernel(
     CacheView C, CacheView M, const int32_t* __restrict__ slot_of_page, const int32_t* __restrict__ pt,
     int64_t max_pages, const int64_t* __restrict__ pos, int n_seqs, int n_tok, const uint16_t* __restrict__ k,
     const uint16_t* __restrict__ v, FastDiv div_h, FastDiv div_tok, FastDiv div_p, int* status) {
@@ -243,10 +243,10 @@ void append_launch(const Launch& L, dim3 grid, dim3 block, const CacheView& C, c
                    const void* v, int split) {
   const FastDiv dh(static_cast<uint32_t>(C.H)), dt(static_cast<uint32_t>(n_tok)), dp(static_cast<uint32_t>(C.P));
   if (BF16 && !split) {
-    // persistent: four 8-warp CTAs per SM, or fewer when the items run out
+    // persistent: three 8-warp CTAs per SM (85 registers a thread), or fewer when the items run out
     const int64_t items = static_cast<int64_t>(n_seqs) * n_tok * C.H;
     const int64_t want = (items + kWarps - 1) / kWarps;
-    const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(want, static_cast<int64_t>(L.num_sms) * 4)));
+    const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(want, static_cast<int64_t>(L.num_sms) * 3)));
     const auto* kb = static_cast<const uint16_t*>(k);
     const auto* vb = static_cast<const uint16_t*>(v);
     if (M) append_bf16_kernel<FMT, true><<<pgrid, block, 0, L.stream>>>(C, *M, slot, pt, max_pages, pos, n_seqs, n_tok, kb, vb, dh, dt, dp, L.status);

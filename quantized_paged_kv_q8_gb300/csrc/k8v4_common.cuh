@@ -152,6 +152,12 @@ int launch_decode_partial(const Launch& L, const CacheView& C, const AttendPlan&
                           const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs,
                           int max_seq_len, int cell_begin, int cell_end, float sm_scale, float* partial, void* ws,
                           uint32_t wait_ns);
+// the team-of-warps TMA verify kernel (k8v4_decode.cu): 2..8 queries per
+// sequence over the K8V4 format with bf16 queries
+bool verify_ws_supported(const CacheView& C, int n_q, int q_dtype);
+AttendPlan plan_verify_ws(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms);
+int launch_verify_ws(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,
+                     const int32_t* steps, int n_seqs, int n_q, int max_seq_len, float sm_scale, float* out, void* ws);
 // the bound of the mbarrier waits in the tensor-memory and TMA kernels (ns; 0: default)
 uint32_t wait_limit_ns();
 // weighted sum of split partials (o[256], m, l rows of 260 floats) -> out, launched programmatically dependent

@@ -760,6 +760,532 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- verify: several queries per sequence
+// The speculative-decoding window of the pull request's "Tests" (a batch of
+// queries per sequence, each with its own step, i.e. visible length), over the
+// k8v4 format with bf16 queries.  The queries read the same cells, so each
+// 16-cell tile is copied once and converted once for all of them:
+//   - a CTA runs kVTeams teams of four warps; a team takes the range's tiles
+//     round robin (team t: tiles t, t + kVTeams, ...), and one lane of the team
+//     keeps kVStages of them in flight with the same TMA copies as decode;
+//   - warp j of a team owns dims [64 j, 64 j + 64): it converts that quarter of
+//     the tile's K codes and computes the partial scores of every query over
+//     those dims (K scale of its half applied), and it converts that quarter of
+//     the V nibbles and accumulates O^T for every query over those dims -- so
+//     the accumulators (4 m-tiles x NQ queries) fit in registers;
+//   - the four partial scores of a (cell, query, head) meet in shared memory;
+//     warp q % 4 owns query q: it sums them (fixed order), masks the cells past
+//     the query's step, runs decode's bucketed softmax and publishes p' (two
+//     fp16 terms in the MMA B layout) with the accumulator rescale factors;
+//   - one named barrier per tile orders the team: after it, the owners run the
+//     softmax of tile u while every warp accumulates PV of tile u - 1 (scores
+//     and p' double-buffered), so the owners' work overlaps the others'.  A
+//     timeout or a bad page never leaves a warp waiting: every warp reaches
+//     the barrier each iteration, and the team leaves the loop together on a
+//     flag its first warp published before the barrier.
+// The partial rows (o, m, l) per (query, head) go to the split combine.
+constexpr int kVTeams = 2;
+constexpr int kVStages = 6;
+constexpr int kVMaxQ = 8;
+
+struct VLayout {
+  int stage_bytes, v_off, ksc_off, vsc_off, tx_bytes;   // the decode stage (K8V4 format)
+  int q_off, x_off, pb_off, flag_off, bar_off, total;
+};
+
+inline VLayout vlayout_of(int H, int nq) {
+  const Layout D = layout_of(K8V4_FORMAT_K8V4, H, 1);
+  VLayout L;
+  L.stage_bytes = D.stage_bytes;
+  L.v_off = D.v_off;
+  L.ksc_off = D.ksc_off;
+  L.vsc_off = D.vsc_off;
+  L.tx_bytes = D.tx_bytes;
+  const int ring = kVTeams * kVStages * L.stage_bytes;
+  L.q_off = ring;                                   // [4 warps][nq][32 lanes][4 k-steps][2 words]
+  L.x_off = L.q_off + 4 * nq * 32 * 8 * 4;          // [2 tiles][team][4 warps][nq][32 lanes][4] f32
+  L.pb_off = L.x_off + 2 * kVTeams * 4 * nq * 32 * 16;   // [2 tiles][team][nq][32 lanes][8 words]
+  const int work_end = L.pb_off + 2 * kVTeams * nq * 32 * 32;
+  const int merge = kVTeams * nq * kGqa * 258 * 4;  // epilogue: [team][nq x 8 rows][258] f32
+  L.flag_off = (std::max(work_end, merge) + 15) & ~15;   // abort word, then two stop words per team
+  L.bar_off = L.flag_off + 32;                      // full barriers [team][stage]
+  L.total = L.bar_off + 8 * kVTeams * kVStages + 1024;
+  return L;
+}
+
+struct VerifyWsParams {
+  CacheView C;
+  const uint16_t* q;       // bf16 [n_seqs][nq][8 H][256]
+  const int32_t* pt;
+  int64_t max_pages;
+  const int32_t* steps;    // [n_seqs][nq]
+  int max_seq_len, cells_per_split, splits;
+  float sm_scale_log2;
+  float* ws;               // partial rows [n_seqs][splits][nq][8 H][260]
+  int* status;
+  uint32_t wait_ns;
+  FastDiv page_div;
+  VLayout L;
+};
+
+template <int NQ>
+__global__ void __launch_bounds__(32 * 4 * kVTeams, 1)
+    verify_ws_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const VerifyWsParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int kOwn = (NQ + 3) / 4;                // queries a warp owns at most
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t sb = (raw_s + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (sb - raw_s);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int team = wid >> 2, j = wid & 3;           // warp j of the team: dims [64 j, 64 j + 64)
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const CacheView& C = p.C;
+  const VLayout& LY = p.L;
+  const int H = C.H, HQ = H * kGqa;
+  const int r0 = lane >> 2, c = lane & 3;
+
+  // visible lengths: every query's (for the tile range), the owned ones kept
+  int n_max = 0;
+  int vis_o[kOwn];
+#pragma unroll
+  for (int k = 0; k < kOwn; ++k) vis_o[k] = 0;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    int v = p.steps[static_cast<int64_t>(b) * NQ + q];
+    if (v < 0 || v > p.max_seq_len) {
+      if (threadIdx.x == 0 && split == 0 && g == 0) record_status(p.status, K8V4_ERANGE);
+      v = v < 0 ? 0 : p.max_seq_len;
+    }
+    n_max = max(n_max, v);
+    if (q % 4 == j) vis_o[q / 4] = v;
+  }
+  const int c_begin = split * p.cells_per_split;
+  const int c_end = min(c_begin + p.cells_per_split, n_max);
+  const int n_tiles = c_end > c_begin ? (c_end - c_begin + 15) >> 4 : 0;
+  const int n_my = n_tiles > team ? (n_tiles - team + kVTeams - 1) / kVTeams : 0;   // tiles team + kVTeams u
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY.flag_off);
+  volatile int* stop_words = reinterpret_cast<volatile int*>(sm + LY.flag_off + 8 + 8 * team);   // [2]
+  const uint32_t full = sb + LY.bar_off + 8 * kVStages * team;   // this team's stage barriers
+  const uint32_t ring = sb + team * kVStages * LY.stage_bytes;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kVTeams * kVStages; ++i) mbar_init(sb + LY.bar_off + 8 * i, 1);
+    *abort_flag = 0;
+    for (int t = 0; t < 2 * kVTeams; ++t) reinterpret_cast<volatile int*>(sm + LY.flag_off + 8)[t] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+
+  // ---- q fragments of every query into shared memory (team 0's warp j writes
+  // the k-steps of dims [64 j, 64 j + 64), read back by warp j of each team),
+  // and the score factors: lane (r0, c) holds head r0's 64 dims 64 i + 16 c + ...
+  float* fq = reinterpret_cast<float*>(sm + LY.pb_off);      // [nq][8] factors, before the P buffer is used
+  if (team == 0) {
+    for (int q = 0; q < NQ; ++q) {
+      const int64_t qrow = ((static_cast<int64_t>(b) * NQ + q) * HQ + g * kGqa + r0) * kD;
+      // the row's largest magnitude (this lane: dims 64 i + 16 c + 0..15; the four lanes of the row)
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow + 64 * i + 16 * c);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint4 raw = src[t];
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(raw.x)), fabsf(bf16_hi(raw.x))),
+                                   fmaxf(fabsf(bf16_lo(raw.y)), fabsf(bf16_hi(raw.y)))));
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(raw.z)), fabsf(bf16_hi(raw.z))),
+                                   fmaxf(fabsf(bf16_lo(raw.w)), fabsf(bf16_hi(raw.w)))));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      const int ex = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 : 0;
+      const int sh = max(-100, min(100, 14 - ex));
+      const float up = ldexpf(1.0f, sh);
+      // k-steps 4 j + jj: dims 64 j + 16 c + 4 jj + (0..3)
+      float qv[16];
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow + 64 * j + 16 * c);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint4 raw = src[t];
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            qv[8 * t + 2 * u] = bf16_lo(wv[u]);
+            qv[8 * t + 2 * u + 1] = bf16_hi(wv[u]);
+          }
+        }
+      }
+      uint32_t wq[8];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(qv[4 * jj + e], up);
+        const __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+        wq[2 * jj] = *reinterpret_cast<const uint32_t*>(&h0);
+        wq[2 * jj + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+      }
+      uint4* dq = reinterpret_cast<uint4*>(sm + LY.q_off + ((j * NQ + q) * 32 + lane) * 32);
+      dq[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+      dq[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+      if (j == 0 && c == 0) fq[q * kGqa + r0] = p.sm_scale_log2 * ldexpf(1.0f, -sh);
+    }
+  }
+  __syncthreads();
+  // the owned queries' score factors for heads 2c, 2c + 1
+  float f0o[kOwn], f1o[kOwn];
+#pragma unroll
+  for (int k = 0; k < kOwn; ++k) {
+    const int q = j + 4 * k;
+    f0o[k] = q < NQ ? fq[q * kGqa + 2 * c] : 0.0f;
+    f1o[k] = q < NQ ? fq[q * kGqa + 2 * c + 1] : 0.0f;
+  }
+  __syncthreads();                                   // fq is overwritten by the P buffer below
+
+  // ---- this team's copies: local tile u -> stage u % kVStages (the decode copies)
+  const int32_t* pt_row = p.pt + static_cast<int64_t>(b) * p.max_pages;
+  int win0 = -1000000, win_page = -1;
+  auto page_of = [&](int u) -> int {         // warp-uniform u; all lanes call
+    if (u < win0 || u >= win0 + 32) {
+      win0 = u;
+      const int cell = c_begin + 16 * (team + kVTeams * (u + lane));
+      const int64_t pidx = static_cast<int64_t>(p.page_div.div(static_cast<uint32_t>(cell)));
+      win_page = (u + lane < n_my && pidx < p.max_pages) ? pt_row[pidx] : -1;
+    }
+    const int page = __shfl_sync(kFull, win_page, u - win0);
+    return (page >= 0 && page < C.n_pages) ? page : -1;
+  };
+  auto issue = [&](int u, int page) {        // team warp 0 only, all lanes call
+    if (lane == 0) {
+      const uint32_t st = ring + (u % kVStages) * LY.stage_bytes;
+      const uint32_t bar = full + 8 * (u % kVStages);
+      if (page >= 0) {
+        const int cell0 = c_begin + 16 * (team + kVTeams * u);
+        const int slot0 = cell0 - static_cast<int>(p.page_div.div(static_cast<uint32_t>(cell0))) * C.P;
+        mbar_expect_tx(bar, LY.tx_bytes);
+        tma_load_4d(st, &tm_k, 0, g, slot0, page, bar);
+        tma_load_4d(st + 2048, &tm_k, 128, g, slot0, page, bar);
+        tma_load_4d(st + LY.v_off, &tm_v, 0, g, slot0, page, bar);
+        const uint8_t* pg = C.pages + static_cast<int64_t>(page) * C.page_bytes;
+        bulk_load(st + LY.ksc_off, pg + C.ks_off() + static_cast<int64_t>(slot0) * 8 * H, 128 * H, bar);
+        bulk_load(st + LY.vsc_off, pg + C.vs_off() + static_cast<int64_t>(slot0) * 16 * H, 256 * H, bar);
+      } else {
+        record_status(p.status, K8V4_ERANGE);
+        mbar_arrive(bar);
+      }
+    }
+  };
+  if (j == 0) {
+    if (lane == 0 && n_my > 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+    }
+    for (int u = 0; u < min(kVStages, n_my); ++u) issue(u, page_of(u));
+  }
+  int issued = min(kVStages, n_my);
+
+  // K fragment addresses of this warp's quarter (decode's i = j), V fragment rows
+  const int rowA = sigma(r0), rowB = 8 + sigma(r0);
+  uint32_t offA, offB;
+  {
+    const int ch = 4 * (j & 1) + c;
+    offA = 2048 * (j >> 1) + rowA * 128 + 16 * (ch ^ (rowA & 7));
+    offB = 2048 * (j >> 1) + rowB * 128 + 16 * (ch ^ (rowB & 7));
+  }
+  const uint32_t ksA = LY.ksc_off + (rowA * H + g) * 8 + 4 * (j >> 1);   // this half's K scale
+  const uint32_t ksB = LY.ksc_off + (rowB * H + g) * 8 + 4 * (j >> 1);
+  const int mi = lane >> 3;
+  const int vcell = 8 * (mi & 1) + sigma(lane & 7);
+  const uint32_t vrow = LY.v_off + vcell * 128;
+  const int vsw = vcell & 7;
+  const int kc4[4] = {sigma(2 * c), sigma(2 * c + 1), 8 + sigma(2 * c), 8 + sigma(2 * c + 1)};
+  uint32_t soff[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) soff[i] = LY.vsc_off + (kc4[i] * H + g) * 16 + 4 * j;   // blocks 2j, 2j + 1
+  const uint32_t qsm = sb + LY.q_off + ((j * NQ) * 32 + lane) * 32;         // + q * 1024
+  // tile u's buffers: (u & 1) * kVTeams + team
+  float* xs0 = reinterpret_cast<float*>(sm + LY.x_off) + static_cast<int64_t>(team) * 4 * NQ * 32 * 4;
+  uint32_t* pb0 = reinterpret_cast<uint32_t*>(sm + LY.pb_off) + static_cast<int64_t>(team) * NQ * 32 * 8;
+  constexpr int kXBuf = kVTeams * 4 * NQ * 32 * 4, kPBuf = kVTeams * NQ * 32 * 8;
+
+  float o[4][NQ][4];                 // m-tiles 4 j .. 4 j + 3 (rotated space) x queries
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) o[mt][q][0] = o[mt][q][1] = o[mt][q][2] = o[mt][q][3] = 0.0f;
+  int M0[kOwn], M1[kOwn];
+  float l0[kOwn], l1[kOwn];
+#pragma unroll
+  for (int k = 0; k < kOwn; ++k) {
+    M0[k] = M1[k] = INT_MIN;
+    l0[k] = l1[k] = 0.0f;
+  }
+  const uint32_t wait_ns = p.wait_ns;
+  const int bar_id = 1 + team;
+
+  bool work_prev = false;
+  for (int u = 0; u <= n_my; ++u) {
+    // iteration u: scores of tile u (u < n_my), then after the barrier the
+    // owners' softmax of tile u beside every warp's PV of tile u - 1
+    const bool have = u < n_my;
+    const int s = u % kVStages;
+    const uint32_t st = ring + s * LY.stage_bytes;
+    float* xs = xs0 + (u & 1) * kXBuf;
+    uint32_t* pb = pb0 + (u & 1) * kPBuf;
+    bool work = false;
+    if (have) {
+      const bool ok = __all_sync(kFull, mbar_wait(full + 8 * s, (u / kVStages) & 1, wait_ns, abort_flag));
+      if (!ok && lane == 0) {
+        *abort_flag = 1;
+        record_status(p.status, K8V4_ECUDA);
+      }
+      work = ok && page_of(u) >= 0;
+    }
+    // ---- partial scores over this warp's 64 dims, every query
+    if (work) {
+      const uint4 ka = lds128(st + offA), kb = lds128(st + offB);
+      const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+      uint32_t a[4][4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        codes_to_f16(wa[jj], a[jj][0], a[jj][2]);
+        codes_to_f16(wb[jj], a[jj][1], a[jj][3]);
+      }
+      const float sA = __uint_as_float(lds32(st + ksA)), sB = __uint_as_float(lds32(st + ksB));
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const uint4 q0 = lds128(qsm + q * 1024), q1 = lds128(qsm + q * 1024 + 16);
+        float e[4] = {0.0f, 0.0f, 0.0f, 0.0f}, f[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16(e, a[0], q0.x, q0.y);
+        mma_f16(f, a[1], q0.z, q0.w);
+        mma_f16(e, a[2], q1.x, q1.y);
+        mma_f16(f, a[3], q1.z, q1.w);
+        *reinterpret_cast<float4*>(xs + ((j * NQ + q) * 32 + lane) * 4) =
+            make_float4(sA * (e[0] + f[0]), sA * (e[1] + f[1]), sB * (e[2] + f[2]), sB * (e[3] + f[3]));
+      }
+    }
+    named_barrier(bar_id, 128);
+    // the stop word of the previous iteration (published before this barrier)
+    if (u >= 1 && stop_words[(u - 1) & 1]) break;
+    if (j == 0) {
+      // every warp is past PV(u - 2): refill that tile's stage with tile u - 2 + kVStages
+      if (u >= 2 && issued < n_my && !*abort_flag) {
+        issue(issued, page_of(issued));
+        ++issued;
+      }
+      if (lane == 0) stop_words[u & 1] = *abort_flag;
+    }
+    // ---- softmax of the owned queries over tile u
+    if (have) {
+      const int cell0 = c_begin + 16 * (team + kVTeams * u);
+#pragma unroll
+      for (int k = 0; k < kOwn; ++k) {
+        const int q = j + 4 * k;
+        if (q >= NQ) continue;
+        float sc[4];
+        {
+          float4 x[4];
+#pragma unroll
+          for (int jw = 0; jw < 4; ++jw) x[jw] = *reinterpret_cast<const float4*>(xs + ((jw * NQ + q) * 32 + lane) * 4);
+          const bool vA = work && cell0 + rowA < vis_o[k], vB = work && cell0 + rowB < vis_o[k];
+          sc[0] = vA ? ((x[0].x + x[1].x) + (x[2].x + x[3].x)) * f0o[k] : -INFINITY;
+          sc[1] = vA ? ((x[0].y + x[1].y) + (x[2].y + x[3].y)) * f1o[k] : -INFINITY;
+          sc[2] = vB ? ((x[0].z + x[1].z) + (x[2].z + x[3].z)) * f0o[k] : -INFINITY;
+          sc[3] = vB ? ((x[0].w + x[1].w) + (x[2].w + x[3].w)) * f1o[k] : -INFINITY;
+        }
+        int nb0 = M0[k], nb1 = M1[k];
+        float g0 = 1.0f, g1 = 1.0f;
+        const bool up0 = sc[0] > 8.0f * M0[k] || sc[2] > 8.0f * M0[k], up1 = sc[1] > 8.0f * M1[k] || sc[3] > 8.0f * M1[k];
+        if (__any_sync(kFull, up0 || up1)) {
+          float t0 = fmaxf(sc[0], sc[2]), t1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, off));
+            t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, off));
+          }
+          nb0 = max(M0[k], static_cast<int>(fminf(fmaxf(ceilf(t0 * 0.125f), -kBucketClamp), kBucketClamp)));
+          nb1 = max(M1[k], static_cast<int>(fminf(fmaxf(ceilf(t1 * 0.125f), -kBucketClamp), kBucketClamp)));
+          g0 = M0[k] == INT_MIN ? 0.0f : pow2i(8 * (M0[k] - nb0));
+          g1 = M1[k] == INT_MIN ? 0.0f : pow2i(8 * (M1[k] - nb1));
+          l0[k] *= g0;
+          l1[k] *= g1;
+          M0[k] = nb0;
+          M1[k] = nb1;
+        }
+        const float rf0 = static_cast<float>(8 * nb0 - 14), rf1 = static_cast<float>(8 * nb1 - 14);
+        float pr[4];
+        pr[0] = ex2(sc[0] - rf0);
+        pr[1] = ex2(sc[1] - rf1);
+        pr[2] = ex2(sc[2] - rf0);
+        pr[3] = ex2(sc[3] - rf1);
+        l0[k] += pr[0] + pr[2];
+        l1[k] += pr[1] + pr[3];
+        const uint32_t h01 = pack_f16(pr[0], pr[1]), h23 = pack_f16(pr[2], pr[3]);
+        const float2 e01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 e23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        const uint32_t q01 = pack_f16(pr[0] - e01.x, pr[1] - e01.y), q23 = pack_f16(pr[2] - e23.x, pr[3] - e23.y);
+        uint4* dst = reinterpret_cast<uint4*>(pb + (q * 32 + lane) * 8);
+        dst[0] = make_uint4(movmatrix_t(h01), movmatrix_t(h23), movmatrix_t(q01), movmatrix_t(q23));
+        dst[1] = make_uint4(__float_as_uint(g0), __float_as_uint(g1), 0u, 0u);
+      }
+    }
+    // ---- PV of tile u - 1 over this warp's dims: rescale, then O^T += V^hat p' per query
+    if (u >= 1 && work_prev) {
+      const uint32_t stp = ring + ((u - 1) % kVStages) * LY.stage_bytes;
+      const uint32_t* pbp = pb0 + ((u - 1) & 1) * kPBuf;
+      uint32_t ph[NQ][4];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const uint4 pp = *reinterpret_cast<const uint4*>(pbp + (q * 32 + lane) * 8);
+        const uint4 gg = *reinterpret_cast<const uint4*>(pbp + (q * 32 + lane) * 8 + 4);
+        ph[q][0] = pp.x; ph[q][1] = pp.y; ph[q][2] = pp.z; ph[q][3] = pp.w;
+        const float g0 = __uint_as_float(gg.x), g1 = __uint_as_float(gg.y);
+        if (__any_sync(kFull, g0 != 1.0f || g1 != 1.0f)) {
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            o[mt][q][0] *= g0; o[mt][q][2] *= g0;
+            o[mt][q][1] *= g1; o[mt][q][3] *= g1;
+          }
+        }
+      }
+      uint32_t R[4];
+      ldmatrix_x4_t(R, stp + vrow + 16 * ((2 * j + (mi >> 1)) ^ vsw));
+      const uint32_t w0 = lds32(stp + soff[0]), w1 = lds32(stp + soff[1]);
+      const uint32_t w2 = lds32(stp + soff[2]), w3 = lds32(stp + soff[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t sel = h ? 0x7632u : 0x5410u;
+        const uint32_t d01 = prmt(w0, w1, sel), d89 = prmt(w2, w3, sel);
+        uint32_t xa[4], xb[4];
+        nibs_to_f16_8th(R[2 * h], xa[0], xa[1], xa[2], xa[3]);
+        nibs_to_f16_8th(R[2 * h + 1], xb[0], xb[1], xb[2], xb[3]);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t ah[4], al[4];
+          mul_split(xa[2 * hf], d01, ah[0], al[0]);
+          mul_split(xa[2 * hf + 1], d01, ah[1], al[1]);
+          mul_split(xb[2 * hf], d89, ah[2], al[2]);
+          mul_split(xb[2 * hf + 1], d89, ah[3], al[3]);
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            float* acc2 = o[2 * h + hf][q];
+            mma_f16(acc2, ah, ph[q][0], ph[q][1]);
+            mma_f16(acc2, ah, ph[q][2], ph[q][3]);
+            mma_f16(acc2, al, ph[q][0], ph[q][1]);
+          }
+        }
+      }
+    }
+    work_prev = work;
+  }
+#pragma unroll
+  for (int k = 0; k < kOwn; ++k) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0[k] += __shfl_xor_sync(kFull, l0[k], off);
+      l1[k] += __shfl_xor_sync(kFull, l1[k], off);
+    }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  __syncthreads();
+  if (*abort_flag) {
+    // copies still in flight land before the stage memory is reused
+    if (j == 0 && lane == 0) {
+      for (int u = max(0, issued - kVStages); u < issued; ++u) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_sleep(full + 8 * (u % kVStages), (u / kVStages) & 1, 20000u) &&
+               global_ns() - t0 < kWaitDefaultNs) {
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // each team's partial: [nq x 8 rows][258] = o[256], bucket, l
+  float* mine = reinterpret_cast<float*>(sm) + static_cast<int64_t>(team) * NQ * kGqa * 258;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int gm = 4 * j + mt;
+      const int d0 = 32 * (gm >> 1) + 16 * (gm & 1) + 2 * r0;
+      *reinterpret_cast<float2*>(mine + (q * kGqa + 2 * c) * 258 + d0) = make_float2(o[mt][q][0], o[mt][q][2]);
+      *reinterpret_cast<float2*>(mine + (q * kGqa + 2 * c + 1) * 258 + d0) = make_float2(o[mt][q][1], o[mt][q][3]);
+    }
+  }
+  if (r0 == 0) {
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+      const int q = j + 4 * k;
+      if (q >= NQ) continue;
+      reinterpret_cast<int*>(mine + (q * kGqa + 2 * c) * 258)[256] = M0[k];
+      reinterpret_cast<int*>(mine + (q * kGqa + 2 * c + 1) * 258)[256] = M1[k];
+      mine[(q * kGqa + 2 * c) * 258 + 257] = l0[k];
+      mine[(q * kGqa + 2 * c + 1) * 258 + 257] = l1[k];
+    }
+  }
+  __syncthreads();
+  // one warp per row: merge the teams at the largest bucket, rotate back, write (o, m, l)
+  const float* part = reinterpret_cast<const float*>(sm);
+  for (int row = wid; row < NQ * kGqa; row += 4 * kVTeams) {
+    int Mx = INT_MIN;
+#pragma unroll
+    for (int t = 0; t < kVTeams; ++t) Mx = max(Mx, reinterpret_cast<const int*>(part + (t * NQ * kGqa + row) * 258)[256]);
+    float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    float L = 0.0f;
+    if (Mx != INT_MIN) {
+#pragma unroll
+      for (int t = 0; t < kVTeams; ++t) {
+        const float* src = part + (t * NQ * kGqa + row) * 258;
+        const int mt = reinterpret_cast<const int*>(src)[256];
+        if (mt == INT_MIN) continue;
+        const float sc2 = pow2i(8 * (mt - Mx));
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float2 x = *reinterpret_cast<const float2*>(src + 8 * lane + e);
+          v[e] += x.x * sc2;
+          v[e + 1] += x.y * sc2;
+        }
+        L += src[257] * sc2;
+      }
+    }
+#pragma unroll
+    for (int hh = 1; hh < 8; hh <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e & hh) continue;
+        const float a = v[e], bb = v[e + hh];
+        v[e] = a + bb;
+        v[e + hh] = a - bb;
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float tt = __shfl_xor_sync(kFull, v[e], m);
+        v[e] = upper ? tt - v[e] : v[e] + tt;
+      }
+    }
+    constexpr float scale = 1.0f / 32768.0f;   // 1/16 of the transform, 2^-11 of p' (2^14) and (n-8)/8 (2^-3)
+    const int q = row / kGqa, h = row % kGqa;
+    float* dst = p.ws + ((((static_cast<int64_t>(b) * p.splits + split) * NQ + q) * HQ) + g * kGqa + h) * kPStride;
+    reinterpret_cast<float4*>(dst + 8 * lane)[0] = make_float4(v[0] * scale, v[1] * scale, v[2] * scale, v[3] * scale);
+    reinterpret_cast<float4*>(dst + 8 * lane)[1] = make_float4(v[4] * scale, v[5] * scale, v[6] * scale, v[7] * scale);
+    if (lane == 0) {
+      dst[256] = Mx == INT_MIN ? -INFINITY : static_cast<float>(8 * Mx);
+      dst[257] = L * (1.0f / 16384.0f);
+    }
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tensor maps
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -924,6 +1450,29 @@ int dispatch(const Launch& L, const DecodeParams& p, int fmt, bool f32, int n_se
   return f32 ? launch_impl<K8V4_FORMAT_INT8, true>(L, p, n_seqs, out, partial)
              : launch_impl<K8V4_FORMAT_INT8, false>(L, p, n_seqs, out, partial);
 }
+
+template <int NQ>
+int launch_verify_ws_n(const Launch& L, const VerifyWsParams& p, int n_seqs, float* out) {
+  CUtensorMap mk, mv;
+  if (!maps_of(p.C, &mk, &mv)) return K8V4_ECUDA;
+  auto kern = verify_ws_kernel<NQ>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.L.total) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return K8V4_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.C.H, n_seqs);
+  cfg.blockDim = dim3(32 * 4 * kVTeams);
+  cfg.dynamicSmemBytes = p.L.total;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mk, mv, p) != cudaSuccess) return K8V4_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return K8V4_ECUDA;
+  return launch_combine(L, p.ws, p.splits, n_seqs, NQ, p.C.H, out);
+}
 }  // namespace
 
 int launch_decode(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
@@ -947,6 +1496,63 @@ int launch_decode_partial(const Launch& L, const CacheView& C, const AttendPlan&
   p.cell_base = cell_begin;
   p.cell_limit = cell_end;
   return dispatch(L, p, C.fmt, q_dtype == K8V4_F32, n_seqs, partial, true);
+}
+
+
+bool verify_ws_supported(const CacheView& C, int n_q, int q_dtype) {
+  return C.fmt == K8V4_FORMAT_K8V4 && q_dtype == K8V4_BF16 && n_q >= 2 && n_q <= kVMaxQ &&
+         C.n_pages < (int64_t(1) << 31) && C.page_bytes < (int64_t(1) << 39);
+}
+
+AttendPlan plan_verify_ws(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
+  AttendPlan pl{};
+  pl.n_q = n_q;
+  pl.n_groups = 1;
+  pl.warps = 4 * kVTeams;
+  const int tiles = std::max(1, (max_seq_len + 15) / 16);
+  // one CTA per SM at a time; about four CTAs per SM over the grid, so that the
+  // splits past a short sequence's end (which return at once) leave no SM idle,
+  // and at least four tiles per team
+  const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
+  int64_t splits = (4ll * num_sms + pairs - 1) / std::max<int64_t>(pairs, 1);
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, std::max(1, tiles / (4 * kVTeams))));
+  const int tps = static_cast<int>((tiles + splits - 1) / splits);
+  pl.cells_per_split = 16 * tps;
+  pl.splits = (tiles + tps - 1) / tps;
+  pl.ws_bytes = static_cast<size_t>(n_seqs) * pl.splits * n_q * C.H * kGqa * kPStride * sizeof(float);
+  return pl;
+}
+
+int launch_verify_ws(const Launch& L, const CacheView& C, const void* q, const int32_t* pt, int64_t max_pages,
+                     const int32_t* steps, int n_seqs, int n_q, int max_seq_len, float sm_scale, float* out, void* ws) {
+  if (n_seqs == 0) return K8V4_OK;
+  const AttendPlan plan = plan_verify_ws(C, n_seqs, n_q, max_seq_len, L.num_sms);
+  VerifyWsParams p;
+  p.C = C;
+  p.q = static_cast<const uint16_t*>(q);
+  p.pt = pt;
+  p.max_pages = max_pages;
+  p.steps = steps;
+  p.max_seq_len = max_seq_len;
+  p.cells_per_split = plan.cells_per_split;
+  p.splits = plan.splits;
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.ws = static_cast<float*>(ws);
+  p.status = L.status;
+  p.wait_ns = wait_limit_ns() ? wait_limit_ns() : kWaitDefaultNs;
+  p.page_div = FastDiv(static_cast<uint32_t>(C.P));
+  p.L = vlayout_of(C.H, n_q);
+  if (p.L.total > kSmemCap + 1024) return K8V4_EINVAL;
+  switch (n_q) {
+    case 2: return launch_verify_ws_n<2>(L, p, n_seqs, out);
+    case 3: return launch_verify_ws_n<3>(L, p, n_seqs, out);
+    case 4: return launch_verify_ws_n<4>(L, p, n_seqs, out);
+    case 5: return launch_verify_ws_n<5>(L, p, n_seqs, out);
+    case 6: return launch_verify_ws_n<6>(L, p, n_seqs, out);
+    case 7: return launch_verify_ws_n<7>(L, p, n_seqs, out);
+    case 8: return launch_verify_ws_n<8>(L, p, n_seqs, out);
+    default: return K8V4_EINVAL;
+  }
 }
 
 }  // namespace k8v4

@@ -135,7 +135,7 @@ def test_verify_irregular_steps(fmt, P, qdt):
     """Verify with irregular per-query steps (0, 1, page and tile edges,
     mid-tile, the whole sequence): three sequences, 7 queries each, every row
     checked; 16-cell pages with fp32 queries (warp-MMA kernel) and 64-cell pages
-    with bf16 queries (tcgen05 kernel for k8v4)."""
+    with bf16 queries (the team-of-warps TMA kernel for k8v4)."""
     seed = synth.config_seed(4) + 77
     H, n_q = 2, 7
     lens = np.array([1500, 33, 700], np.int32)

@@ -802,16 +802,20 @@ int launch_impl(const Launch& L, const AttendParams& p, const AttendPlan& plan, 
 
 }  // namespace
 
-AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
+namespace {
+AttendPlan plan_attend_base(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
   // several queries per sequence over a k8v4 cache: tiles dequantised once and
   // shared by all queries -- on the tcgen05 kernel (bf16 q, pages of 64k cells)
   // or on the warp-MMA verify kernel; the workspace covers either
   if (n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) {
-    // bf16 queries run the team-of-warps TMA kernel, fp32 queries the warp-MMA
-    // one; the workspace covers either
+    // bf16 queries run the tcgen05 prefill kernel split over cells (pages of a
+    // multiple of 64 cells) or the team-of-warps TMA kernel, fp32 queries the
+    // warp-MMA one; the workspace covers each
     AttendPlan mw = plan_verify(C, n_seqs, n_q, max_seq_len, num_sms);
     if (verify_ws_supported(C, n_q, K8V4_BF16))
       mw.ws_bytes = std::max(mw.ws_bytes, plan_verify_ws(C, n_seqs, n_q, max_seq_len, num_sms).ws_bytes);
+    if (C.P % 64 == 0)
+      mw.ws_bytes = std::max(mw.ws_bytes, plan_verify_tc(C, n_seqs, n_q, max_seq_len, num_sms).ws_bytes);
     return mw;
   }
   if (n_q == 1 && decode_ws_supported(C)) return plan_decode(C, n_seqs, max_seq_len, num_sms);
@@ -837,11 +841,21 @@ AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len,
   return pl;
 }
 
+}  // namespace
+
+AttendPlan plan_attend(const CacheView& C, int n_seqs, int n_q, int max_seq_len, int num_sms) {
+  return plan_attend_base(C, n_seqs, n_q, max_seq_len, num_sms);
+}
+
 int launch_attend(const Launch& L, const CacheView& C, const AttendPlan& plan, const void* q, int q_dtype,
                   const int32_t* pt, int64_t max_pages, const int32_t* steps, int n_seqs, int max_seq_len,
                   float sm_scale, float* out, void* ws, const void* k_new, const void* v_new, int kv_dtype) {
   if (n_seqs == 0) return K8V4_OK;
   if (plan.n_q > 1 && C.fmt == K8V4_FORMAT_K8V4) {
+    if (q_dtype == K8V4_BF16 && C.P % 64 == 0) {
+      const AttendPlan tp = plan_verify_tc(C, n_seqs, plan.n_q, max_seq_len, L.num_sms);
+      return launch_verify_tc(L, C, tp, q, pt, max_pages, steps, n_seqs, max_seq_len, sm_scale, out, ws);
+    }
     if (verify_ws_supported(C, plan.n_q, q_dtype))
       return launch_verify_ws(L, C, q, pt, max_pages, steps, n_seqs, plan.n_q, max_seq_len, sm_scale, out, ws);
     const AttendPlan mw = plan_verify(C, n_seqs, plan.n_q, max_seq_len, L.num_sms);

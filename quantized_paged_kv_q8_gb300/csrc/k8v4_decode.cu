@@ -1303,15 +1303,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // A run of rows [P][H][row_bytes] per page, as a 4-D byte tensor (byte, head,
-// cell, page) with 16-cell x 128-byte boxes, 128-byte swizzled.
-bool encode_rows(CUtensorMap* m, const CacheView& C, int64_t run_off, int row_bytes) {
+// cell, page) with box_rows-cell x 128-byte boxes, 128-byte swizzled.
+bool encode_rows(CUtensorMap* m, const CacheView& C, int64_t run_off, int row_bytes, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(C.H),
                               static_cast<cuuint64_t>(C.P), static_cast<cuuint64_t>(C.n_pages)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(row_bytes) * C.H,
                                  static_cast<cuuint64_t>(C.page_bytes)};
-  const cuuint32_t box[4] = {128, 1, 16, 1};
+  const cuuint32_t box[4] = {128, 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, C.pages + run_off, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1324,25 +1324,26 @@ constexpr int kMapCache = 64;
 struct MapEntry {
   const uint8_t* pages = nullptr;
   int64_t n_pages = 0;
-  int P = 0, H = 0, fmt = 0;
+  int P = 0, H = 0, fmt = 0, box = 0;
   CUtensorMap k, v;
 };
 std::mutex g_map_mu;
 MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
-bool maps_of(const CacheView& C, CUtensorMap* k, CUtensorMap* v) {
+bool maps_of(const CacheView& C, CUtensorMap* k, CUtensorMap* v, int box_rows = 16) {
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (const MapEntry& e : g_maps) {
-    if (e.pages == C.pages && e.n_pages == C.n_pages && e.P == C.P && e.H == C.H && e.fmt == C.fmt) {
+    if (e.pages == C.pages && e.n_pages == C.n_pages && e.P == C.P && e.H == C.H && e.fmt == C.fmt &&
+        e.box == box_rows) {
       *k = e.k;
       *v = e.v;
       return true;
     }
   }
   MapEntry& e = g_maps[g_map_next];
-  if (!encode_rows(&e.k, C, 0, 256) ||
-      !encode_rows(&e.v, C, C.v_off(), C.fmt == K8V4_FORMAT_INT8 ? 256 : 128)) {
+  if (!encode_rows(&e.k, C, 0, 256, box_rows) ||
+      !encode_rows(&e.v, C, C.v_off(), C.fmt == K8V4_FORMAT_INT8 ? 256 : 128, box_rows)) {
     e.pages = nullptr;
     return false;
   }
@@ -1351,6 +1352,7 @@ bool maps_of(const CacheView& C, CUtensorMap* k, CUtensorMap* v) {
   e.P = C.P;
   e.H = C.H;
   e.fmt = C.fmt;
+  e.box = box_rows;
   g_map_next = (g_map_next + 1) % kMapCache;
   *k = e.k;
   *v = e.v;

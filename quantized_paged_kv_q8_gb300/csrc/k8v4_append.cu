@@ -84,10 +84,10 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(CacheView C, CacheV
 
 // ------------------------------------------------------------------ bulk bf16 append
 // The long appends of bf16 rows (a prompt chunk, a cache build): a persistent
-// grid of 8-warp CTAs, each warp striding over (seq, token, head) items; the
-// warp loads the next item's K and V rows (16 B per lane each) before it
-// quantises the current one, so every warp keeps 1 KB of loads in flight while
-// it computes.  The rows are quantised by the bf16 fast paths (int8 K, exact
+// grid of 8-warp CTAs, each warp stepping through a contiguous run of (seq,
+// token, head) items; the warp loads the next item's K and V rows (16 B per
+// lane each) before it quantises the current one, so every warp keeps 1 KB of
+// loads in flight while it computes.  The rows are quantised by the bf16 fast paths (int8 K, exact
 // rotation + q4_0 V, same bytes as append_kernel).
 template <int FMT, bool MIRROR>
 __global__ void __launch_bounds__(kWarps * 32, 3) append_bf16_kernel(
@@ -101,58 +101,78 @@ __global__ void __launch_bounds__(kWarps * 32, 3) append_bf16_kernel(
   long long* ts = stage[w];
   fill_int8_scale_table(scale_tab);
   __syncthreads();
-  // the host keeps total below 2^31, and a cell that passes the range check is
-  // below max_pages * P <= 2^31, so the index arithmetic runs in 32 bits
+  // Each warp takes a contiguous run of (seq, token, head) items and steps
+  // through it: the head, token and sequence indices advance by increments, and
+  // the page lookup is redone only when a token crosses into another page or
+  // sequence.  The host keeps total below 2^31, and a cell that passes the range
+  // check is below max_pages * P <= 2^31, so the index arithmetic runs in 32 bits.
   const uint32_t total = static_cast<uint32_t>(n_seqs) * static_cast<uint32_t>(n_tok) * static_cast<uint32_t>(C.H);
-  const uint32_t stride = gridDim.x * kWarps;
-  uint32_t item = blockIdx.x * kWarps + w;
-  uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
-  if (item < total) {
-    kr = __ldcs(reinterpret_cast<const uint4*>(k + static_cast<int64_t>(item) * kD) + lane);
-    vr = __ldcs(reinterpret_cast<const uint4*>(v + static_cast<int64_t>(item) * kD) + lane);
-  }
-  for (; item < total; item += stride) {
+  const uint32_t n_warps = gridDim.x * kWarps;
+  const uint32_t per = (total + n_warps - 1) / n_warps;
+  uint32_t item = (blockIdx.x * kWarps + w) * per;
+  const uint32_t item_end = min(item + per, total);
+  if (item >= item_end) return;
+  const uint4* kp = reinterpret_cast<const uint4*>(k + static_cast<int64_t>(item) * kD) + lane;
+  const uint4* vp = reinterpret_cast<const uint4*>(v + static_cast<int64_t>(item) * kD) + lane;
+  uint4 kr = __ldcs(kp), vr = __ldcs(vp);
+  const uint32_t it0 = div_h.div(item);
+  int g = static_cast<int>(item - it0 * static_cast<uint32_t>(C.H));
+  uint32_t b = div_tok.div(it0);
+  int t = static_cast<int>(it0 - b * static_cast<uint32_t>(n_tok));
+  const int64_t cell_limit = max_pages * C.P;
+  int64_t cell = pos[b] + t;
+  bool lookup = true;                   // the page of `cell` must be looked up
+  int cslot = 0;
+  uint8_t* base = nullptr;
+  uint8_t* base2 = nullptr;
+  for (; item < item_end; ++item) {
     const uint4 kc = kr, vc = vr;
-    const uint32_t next = item + stride;
-    if (next < total) {
-      kr = __ldcs(reinterpret_cast<const uint4*>(k + static_cast<int64_t>(next) * kD) + lane);
-      vr = __ldcs(reinterpret_cast<const uint4*>(v + static_cast<int64_t>(next) * kD) + lane);
+    if (item + 1 < item_end) {
+      kp += kD / 8;
+      vp += kD / 8;
+      kr = __ldcs(kp);
+      vr = __ldcs(vp);
     }
-    const uint32_t it = div_h.div(item);
-    const int g = static_cast<int>(item - it * static_cast<uint32_t>(C.H));
-    const uint32_t b = div_tok.div(it);
-    const int t = static_cast<int>(it - b * static_cast<uint32_t>(n_tok));
-    const int64_t cell = pos[b] + t;
-    if (cell < 0 || cell >= max_pages * C.P) {
+    const bool in_range = cell >= 0 && cell < cell_limit;
+    if (in_range && lookup) {
+      const uint32_t pidx = div_p.div(static_cast<uint32_t>(cell));
+      cslot = static_cast<int>(static_cast<uint32_t>(cell) - pidx * static_cast<uint32_t>(C.P));
+      const int64_t page = pt[static_cast<int64_t>(b) * max_pages + pidx];
+      base = nullptr;
+      base2 = nullptr;
+      if (MIRROR) {
+        if (page >= 0 && page < M.n_pages) {
+          base = M.pages + page * M.page_bytes;
+          const int dslot = slot_of_page[page];
+          if (dslot >= 0 && dslot < C.n_pages) base2 = C.pages + static_cast<int64_t>(dslot) * C.page_bytes;
+          else if (dslot != -1 && lane == 0) record_status(status, K8V4_ERANGE);
+        }
+      } else if (page >= 0 && page < C.n_pages) {
+        base = C.pages + page * C.page_bytes;
+      }
+      lookup = false;
+    }
+    if (!in_range || base == nullptr) {
       if (lane == 0) record_status(status, K8V4_ERANGE);
-      continue;
-    }
-    const uint32_t pidx = div_p.div(static_cast<uint32_t>(cell));
-    const int cslot = static_cast<int>(static_cast<uint32_t>(cell) - pidx * static_cast<uint32_t>(C.P));
-    const int64_t page = pt[static_cast<int64_t>(b) * max_pages + pidx];
-    const int64_t r = static_cast<int64_t>(cslot) * C.H + g;
-    uint8_t* base;
-    uint8_t* base2 = nullptr;
-    if (MIRROR) {
-      if (page < 0 || page >= M.n_pages) {
-        if (lane == 0) record_status(status, K8V4_ERANGE);
-        continue;
-      }
-      base = M.pages + page * M.page_bytes;
-      const int dslot = slot_of_page[page];
-      if (dslot >= 0 && dslot < C.n_pages) base2 = C.pages + static_cast<int64_t>(dslot) * C.page_bytes;
-      else if (dslot != -1 && lane == 0) record_status(status, K8V4_ERANGE);
     } else {
-      if (page < 0 || page >= C.n_pages) {
-        if (lane == 0) record_status(status, K8V4_ERANGE);
-        continue;
-      }
-      base = C.pages + page * C.page_bytes;
+      const int r = cslot * C.H + g;
+      if (FMT == K8V4_FORMAT_Q4) rot_q4_row_bf16(kc, lane, ts, base, base2, r * 128, C.ks_off() + r * 16);
+      else int8_row_bf16(kc, lane, scale_tab, base, base2, r * 256, C.ks_off() + r * 8);
+      if (FMT == K8V4_FORMAT_INT8) int8_row_bf16(vc, lane, scale_tab, base, base2, C.v_off() + r * 256, C.vs_off() + r * 8);
+      else rot_q4_row_bf16(vc, lane, ts, base, base2, C.v_off() + r * 128, C.vs_off() + r * 16);
     }
-    if (FMT == K8V4_FORMAT_Q4) rot_q4_row_bf16(kc, lane, ts, base, base2, r * 128, C.ks_off() + r * 16);
-    else int8_row_bf16(kc, lane, scale_tab, base, base2, r * 256, C.ks_off() + r * 8);
-    if (FMT == K8V4_FORMAT_INT8) int8_row_bf16(vc, lane, scale_tab, base, base2, C.v_off() + r * 256, C.vs_off() + r * 8);
-    else rot_q4_row_bf16(vc, lane, ts, base, base2, C.v_off() + r * 128, C.vs_off() + r * 16);
+    // the next item: head, then token (its cell), then sequence
+    if (++g == C.H) {
+      g = 0;
+      if (++t == n_tok) {
+        t = 0;
+        if (++b < static_cast<uint32_t>(n_seqs)) cell = pos[b];
+        lookup = true;
+      } else {
+        ++cell;
+        if (++cslot == C.P) lookup = true;
+      }
+    }
   }
 }
 

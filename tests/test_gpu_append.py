@@ -268,3 +268,32 @@ def test_append_bf16_fast_path_edges(fmt):
     torch.cuda.synchronize()
     assert k8.k8v4_last_device_status() == 0
     _assert_bytes_equal(gpu, ref)
+
+
+def test_append_bf16_bulk_bad_page_is_skipped_and_reported():
+    """The persistent bf16 kernel (a long append) over a page table with one bad
+    id: the cells of that page are skipped and K8V4_ERANGE is recorded; every
+    other cell's bytes equal the oracle's, including cells after the bad page."""
+    n, P = 1024, 64
+    rng = np.random.default_rng(31)
+    k = synth.Tensor(rng.standard_normal((1, n, 2, 256)).astype(np.float32), "bf16")
+    v = synth.Tensor(rng.standard_normal((1, n, 2, 256)).astype(np.float32), "bf16")
+    n_pages = n // P
+    perm = np.random.default_rng(32).permutation(n_pages).astype(np.int32)
+    pt = perm.copy()[None]
+    pt[0, 5] = n_pages + 7                                  # page index 5 -> a bad id
+    gpu, ref = make_caches(n_pages, P)
+    pt_d = torch.from_numpy(pt).cuda()
+    k8.kv_append_k8v4(gpu, pt_d, torch.zeros(1, dtype=torch.int64, device="cuda"), dev_tensor(k), dev_tensor(v))
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == k8.ERANGE
+    assert k8.k8v4_last_device_status() == 0
+    ok = perm[None].copy()
+    ref.append(ok, np.array([0]), k.f32[:, :5 * P], v.f32[:, :5 * P])
+    ref.append(ok, np.array([6 * P]), k.f32[:, 6 * P:], v.f32[:, 6 * P:])
+    got = gpu.pages.cpu().numpy()
+    # the page the bad entry would have used stays a canary
+    assert np.all(got.reshape(n_pages, -1)[perm[5]] == CANARY)
+    mask = np.ones(n_pages, bool)
+    mask[perm[5]] = False
+    assert np.array_equal(got.reshape(n_pages, -1)[mask], ref.buf.reshape(n_pages, -1)[mask])

@@ -182,7 +182,7 @@ def test_verify_rows_equal_decode_at_step():
 
 def test_verify_config4_full_sampled():
     """Config 4 at full size: 8 sequences, lengths U[16,384, 65,536], 5 queries
-    each; sampled rows (queries 0 and 4, heads 0, 7, 8, 15 of every sequence)."""
+    each; every one of the 640 rows (8 sequences x 5 queries x 16 heads)."""
     w = synth.config4()
     gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv)
     pt_d = torch.from_numpy(w.page_table).cuda()
@@ -192,7 +192,7 @@ def test_verify_config4_full_sampled():
     q = torch.stack([dev_tensor(w.q[b]) for b in range(w.n_seqs)])
     got = verify_gpu(gpu, q, pt_d, w.steps, int(w.seq_lens.max()))
     assert k8.k8v4_last_device_status() == 0
-    sel = [(b, i, h) for b in range(w.n_seqs) for i in (0, 4) for h in (0, 7, 8, 15)]
+    sel = [(b, i, h) for b in range(w.n_seqs) for i in range(w.n_q) for h in range(16)]
     rs = np.array([s[0] for s in sel], np.int32)
     rh = np.array([s[2] for s in sel], np.int32)
     rv = np.array([w.steps[b, i] for b, i, _ in sel], np.int32)

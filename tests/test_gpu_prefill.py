@@ -107,7 +107,8 @@ def test_prefill_rows_equal_decode():
 def test_prefill_config5_full_sampled():
     """Config 5: append an 8,192-token chunk at offset 229,376 (after the 229,376-cell
     history), then causal prefill of the chunk over 237,568 cells; the appended
-    chunk's bytes are checked in full, attention on sampled rows."""
+    chunk's bytes are checked in full, attention on 540 rows: the edge tokens and
+    one seeded row in each of the 512 token blocks."""
     w = synth.config5()
     gpu, ref = make_caches(w.n_pages, w.page_size, w.n_kv)
     hk, hv = synth.prefill_kv(w, 0, w.history)
@@ -122,12 +123,15 @@ def test_prefill_config5_full_sampled():
     q = synth.prefill_q(w)
     got = _prefill(gpu, dev_tensor(q, (w.chunk, 16, 256)), pt_d[0], w.total)
     assert k8.k8v4_last_device_status() == 0
-    toks = [0, 1, 15, 16, 1000, 4095, 8191]
-    heads = [0, 7, 8, 15]
-    rs = np.zeros(len(toks) * len(heads), np.int32)
-    rh = np.array([h for _ in toks for h in heads], np.int32)
-    rv = np.array([w.history + t + 1 for t in toks for _ in heads], np.int32)
-    qrows = np.stack([q.f32[t, h] for t in toks for h in heads])
+    # hand-picked edges, plus one seeded (token, head) row in every 16-token block
+    # (every CTA row group and both KV heads' CTAs), 540 rows in all
+    sel = [(t, h) for t in (0, 1, 15, 16, 1000, 4095, 8191) for h in (0, 7, 8, 15)]
+    rng = np.random.default_rng(20251)
+    sel += [(16 * blk + int(rng.integers(16)), int(rng.integers(16))) for blk in range(w.chunk // 16)]
+    rs = np.zeros(len(sel), np.int32)
+    rh = np.array([h for _, h in sel], np.int32)
+    rv = np.array([w.history + t + 1 for t, _ in sel], np.int32)
+    qrows = np.stack([q.f32[t, h] for t, h in sel])
     want = ref.attention(w.page_table, rs, rh, rv, qrows)
-    gsel = np.stack([got[t, h] for t in toks for h in heads])
+    gsel = np.stack([got[t, h] for t, h in sel])
     assert rel_err(gsel, want) <= TOL

@@ -1400,14 +1400,18 @@ AttendPlan plan_decode(const CacheView& C, int n_seqs, int max_seq_len, int num_
   const int tiles = std::max(1, (max_seq_len + 15) / 16);
   const int64_t pairs = static_cast<int64_t>(C.H) * n_seqs;
   // one CTA per SM: split each (sequence, KV head) into the number of cell
-  // ranges that minimises waves x tiles per range (each range keeps at least
-  // 2 tiles per worker warp)
+  // ranges that minimises waves x (tiles per range + a CTA's fixed cost), each
+  // range keeping at least 2 tiles per worker warp.  The fixed cost (q set-up,
+  // pipeline fill, the workers' merge) is worth about kCtaFixedTiles tiles of
+  // a CTA's streaming: without it, 32 sequences of 8,192 cells chose 8 waves of
+  // 27-tile CTAs (120 us) over one wave of 256-tile CTAs (75 us).
+  constexpr int kCtaFixedTiles = 32;
   const int max_splits = std::max(1, std::min(1024, tiles / (2 * kMaxWorkers)));
   int64_t best_cost = INT64_MAX;
   int best = 1;
   for (int sp = 1; sp <= max_splits; ++sp) {
     const int64_t waves = (pairs * sp + num_sms - 1) / num_sms;
-    const int64_t cost = waves * ((tiles + sp - 1) / sp);
+    const int64_t cost = waves * ((tiles + sp - 1) / sp + kCtaFixedTiles);
     if (cost < best_cost) {
       best_cost = cost;
       best = sp;

@@ -339,11 +339,13 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
         const int64_t r = static_cast<int64_t>(cell % C.P) * H + g;
         const int64_t elem = (static_cast<int64_t>(b) * H + g) * kD + 8 * lane;
         long long* ts = reinterpret_cast<long long*>(sm) + w * kRotScratch;   // stage memory, not yet in use
+        // bf16 rows take the bulk append's fast paths (same bytes, fewer
+        // instructions: this CTA's copies wait for them)
         if (w == 0) {
-          if (p.kv_bf16) append_k_row<true, FMT>(C, base, r, p.k_new, elem, lane, ts);
+          if (p.kv_bf16) append_k_row_bf16<FMT>(C, base, r, static_cast<const uint16_t*>(p.k_new) + elem - 8 * lane, lane, ts);
           else append_k_row<false, FMT>(C, base, r, p.k_new, elem, lane, ts);
         } else {
-          if (p.kv_bf16) append_v_row<true, FMT>(C, base, r, p.v_new, elem, lane, ts);
+          if (p.kv_bf16) append_v_row_bf16<FMT>(C, base, r, static_cast<const uint16_t*>(p.v_new) + elem - 8 * lane, lane, ts);
           else append_v_row<false, FMT>(C, base, r, p.v_new, elem, lane, ts);
         }
       } else if (w == 0 && lane == 0) {

@@ -644,5 +644,37 @@ __device__ __forceinline__ void rot_q4_row_bf16(const uint4 raw, int lane, long 
   if ((lane & 3) == 0) st2(a, b, s_off + 2 * (lane >> 2), dh);
 }
 
+// One bf16 row of a single-token append (the fused decode step) through the
+// fast paths above: K as int8 (its scale table first built by the warp in ts),
+// or rotated q4_0 in the Q4 format; V as rotated q4_0, or int8 in the INT8
+// format.  src points at the row's first element (16-byte aligned); same bytes
+// as append_k_row / append_v_row.
+template <int FMT>
+__device__ __forceinline__ void append_k_row_bf16(const CacheView& C, uint8_t* base, int64_t r, const uint16_t* src,
+                                                  int lane, long long* ts) {
+  const uint4 raw = reinterpret_cast<const uint4*>(src)[lane];
+  if (FMT == K8V4_FORMAT_Q4) {
+    rot_q4_row_bf16(raw, lane, ts, base, nullptr, r * 128, C.ks_off() + r * 16);
+    return;
+  }
+  float* tab = reinterpret_cast<float*>(ts);
+  for (int i = lane; i < 128; i += 32) tab[i] = __fdiv_rn(static_cast<float>(128 + i), 127.0f);
+  __syncwarp();
+  int8_row_bf16(raw, lane, tab, base, nullptr, r * 256, C.ks_off() + r * 8);
+}
+template <int FMT>
+__device__ __forceinline__ void append_v_row_bf16(const CacheView& C, uint8_t* base, int64_t r, const uint16_t* src,
+                                                  int lane, long long* ts) {
+  const uint4 raw = reinterpret_cast<const uint4*>(src)[lane];
+  if (FMT != K8V4_FORMAT_INT8) {
+    rot_q4_row_bf16(raw, lane, ts, base, nullptr, C.v_off() + r * 128, C.vs_off() + r * 16);
+    return;
+  }
+  float* tab = reinterpret_cast<float*>(ts);
+  for (int i = lane; i < 128; i += 32) tab[i] = __fdiv_rn(static_cast<float>(128 + i), 127.0f);
+  __syncwarp();
+  int8_row_bf16(raw, lane, tab, base, nullptr, C.v_off() + r * 256, C.vs_off() + r * 8);
+}
+
 }  // namespace
 }  // namespace k8v4

@@ -120,3 +120,29 @@ def test_decode_step_config3_full():
     rs, rh, rv = oracle.decode_rows(1, 16, w.seq_lens)
     want = ref.attention(w.page_table, rs, rh, rv, w.q.f32.reshape(-1, 256))
     assert rel_err(out.cpu().numpy().reshape(-1, 256), want) <= TOL
+
+
+def test_decode_step_many_sequences():
+    """The engine's batched shape at scale: 40 sequences of seeded ragged lengths
+    (80 (sequence, KV head) pairs, more than half the SMs, so the split plan
+    trades ranges per pair against waves), pages interleaved in one pool.  The
+    fused step appends every newest token and attends; cache bytes and every
+    row against the oracle."""
+    rng = np.random.default_rng(synth.config_seed(3) + 777)
+    lens = rng.integers(700, 6000, size=40).astype(np.int32)
+    lens[3] = 1
+    lens[11] = 64
+    pt, lens, q, _, gpu_b, ref, k_new, v_new = _setup(k8.FORMAT_K8V4, "bf16", lens, seed_off=7)
+    n = len(lens)
+    max_len = int(lens.max())
+    pt_d = torch.from_numpy(pt).cuda()
+    out = torch.empty(n, 16, 256, dtype=torch.float32, device="cuda")
+    ws = k8.workspace(gpu_b, n, 1, max_len)
+    k8.attn_k8v4_decode_step(gpu_b, dev_tensor(q, (n, 16, 256)), dev_tensor(k_new, (n, 2, 256)),
+                             dev_tensor(v_new, (n, 2, 256)), pt_d, torch.from_numpy(lens).cuda(), max_len, out, ws)
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    assert np.array_equal(gpu_b.pages.cpu().numpy(), ref.buf)
+    rs, rh, rv = oracle.decode_rows(n, 16, lens)
+    want = ref.attention(pt, rs, rh, rv, q.f32.reshape(-1, 256))
+    assert rel_err(out.cpu().numpy().reshape(-1, 256), want) <= TOL

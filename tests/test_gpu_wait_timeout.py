@@ -12,7 +12,7 @@ import torch
 import oracle
 import quantized_paged_kv_q8_gb300 as k8
 import synth
-from gpu_util import TOL, append_both, decode_gpu, dev_tensor, make_caches, rel_err
+from gpu_util import TOL, append_both, decode_gpu, dev_tensor, make_caches, rel_err, verify_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -79,5 +79,41 @@ def test_decode_wait_timeout_then_recovery(qdt):
     got = decode_gpu(gpu, q_d, pt_d, w.seq_lens, n)
     assert k8.k8v4_last_device_status() == 0
     rs, rh, rv = oracle.decode_rows(1, 16, w.seq_lens)
+    want = ref.attention(w.page_table, rs, rh, rv, q.f32.reshape(-1, 256))
+    assert rel_err(got.reshape(-1, 256), want) <= TOL
+
+
+def test_verify_team_kernel_wait_timeout_then_recovery():
+    """The team-of-warps verify kernel (bf16 queries, pages that are not a
+    multiple of 64 cells): the same bounded-wait failure path, then a normal
+    call in the same process against the oracle."""
+    n, P, n_q = 32768, 16, 3
+    w = synth.decode_workload(synth.config_seed(4) + 903, n, P=P, name="timeout-verify")
+    gpu, ref = make_caches(w.n_pages, P, 2)
+    pt_d = append_both(gpu, ref, w.page_table, w.pos, synth.Tensor(w.k.f32[None], "bf16"),
+                       synth.Tensor(w.v.f32[None], "bf16"))
+    q = synth.q_values(w.seed, 9, n_q, 2, "bf16")
+    q_d = dev_tensor(q, (1, n_q, 16, 256))
+    steps = np.array([[n - 2, n - 1, n]], np.int32)
+    assert k8.k8v4_last_device_status() == 0
+    flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+    statuses = []
+    try:
+        for _ in range(5):
+            float(flush.sum())
+            torch.cuda.synchronize()
+            k8.k8v4_set_wait_limit_ns(1)
+            verify_gpu(gpu, q_d, pt_d, steps, n)
+            k8.k8v4_set_wait_limit_ns(0)
+            statuses.append(k8.k8v4_last_device_status())
+            if statuses[-1] == k8.ECUDA:
+                break
+    finally:
+        k8.k8v4_set_wait_limit_ns(0)
+    assert statuses[-1] == k8.ECUDA and set(statuses) <= {0, k8.ECUDA}, statuses
+    del flush
+    got = verify_gpu(gpu, q_d, pt_d, steps, n)
+    assert k8.k8v4_last_device_status() == 0
+    rs, rh, rv = oracle.multi_query_rows(steps, 16)
     want = ref.attention(w.page_table, rs, rh, rv, q.f32.reshape(-1, 256))
     assert rel_err(got.reshape(-1, 256), want) <= TOL

@@ -5,10 +5,13 @@
 // write the merged partial itself (o, M, L unnormalised), which is what one GPU
 // of a cell-range split hands to the others.
 //
-// One CTA per (row, 32-dim chunk), eight warps.  Warp w folds splits w, w + 8,
-// ... into a running (M, L, acc) with the online-softmax update, so every load
-// of a split is independent of the others (no separate maximum pass); the eight
-// warp states are merged in shared memory.  Launched as a programmatic
+// One CTA per (row, 32-dim chunk), eight warps.  Warp w takes splits w, w + 8,
+// ... in rounds of kRound: every load of a round (each split's m and l, and the
+// lane's element of o) is issued before any is used, so a round costs one L2
+// round trip; the round is folded at its own maximum into the warp's running
+// (M, L, acc), and the eight warp states are merged in shared memory.  A long
+// single-sequence decode (76 splits per KV head on 152 SMs) takes one round;
+// 12 splits of a warp fit 64 registers, four CTAs per SM.  Launched as a programmatic
 // dependent of the split kernel: the launch overlaps the split kernel's tail and
 // griddepcontrol.wait holds the loads until the partials are written.
 #include "k8v4_common.cuh"
@@ -17,10 +20,11 @@ namespace k8v4 {
 namespace {
 
 constexpr int kPStride = 260;   // floats per partial row: o[256], m, l, 2 pad
+constexpr int kRound = 12;      // splits per warp whose loads are in flight together
 
 // row r = (b, rr) with rr < rows_per_b; split s of row r at
 // src + b * b_stride + s * split_stride + rr * kPStride
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ src, int splits, int64_t split_stride,
+__global__ void __launch_bounds__(256, 4) combine_kernel(const float* __restrict__ src, int splits, int64_t split_stride,
                                                       int64_t b_stride, int rows_per_b, float* __restrict__ out,
                                                       int write_partial) {
   __shared__ float wm[8], wl[8], wacc[8][32];
@@ -31,16 +35,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const float* base = src + b * b_stride + static_cast<int64_t>(rr) * kPStride;
   const int dim = chunk * 32 + lane;
   float M = -INFINITY, L = 0.0f, acc = 0.0f;
-#pragma unroll 4
-  for (int s = warp; s < splits; s += 8) {
-    const float* p = base + s * split_stride;
-    const float ms = p[256], ls = p[257], x = p[dim];
-    if (ms == -INFINITY) continue;                     // nothing visible in this split
-    const float mn = fmaxf(M, ms);
-    const float a = exp2f(M - mn), w = exp2f(ms - mn);  // a = 0 while M = -inf
-    acc = acc * a + x * w;
-    L = L * a + ls * w;
-    M = mn;
+  for (int s0 = warp; s0 < splits; s0 += 8 * kRound) {
+    float ms[kRound], ls[kRound], xs[kRound];
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {
+      const int s = s0 + 8 * k;
+      ms[k] = -INFINITY;
+      ls[k] = xs[k] = 0.0f;
+      if (s < splits) {
+        const float* p = base + s * split_stride;
+        ms[k] = p[256];
+        ls[k] = p[257];
+        xs[k] = p[dim];
+      }
+    }
+    float mr = M;
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) mr = fmaxf(mr, ms[k]);
+    if (mr == -INFINITY) continue;                      // nothing visible yet (the same for the warp)
+    const float a = exp2f(M - mr);                      // 0 while M = -inf
+    acc *= a;
+    L *= a;
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {
+      if (ms[k] == -INFINITY) continue;                 // a split with nothing visible
+      const float wk = exp2f(ms[k] - mr);
+      acc += xs[k] * wk;
+      L += ls[k] * wk;
+    }
+    M = mr;
   }
   if (lane == 0) {
     wm[warp] = M;

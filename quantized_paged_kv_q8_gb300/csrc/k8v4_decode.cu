@@ -55,6 +55,13 @@ constexpr int kPStride = 260;                          // floats per partial row
 constexpr uint32_t kWaitDefaultNs = 1000000000u;       // 1 s
 constexpr int kBucketClamp = 1 << 24;
 constexpr int kSmemCap = 227 * 1024;
+// A worker's partial in the epilogue: [8 heads][kHeadStride] floats of o, then 8
+// buckets and 8 sums.  A head stride of 4 mod 16 floats puts the four lane
+// groups of one fragment store in four different bank octets.
+constexpr int kHeadStride = 260;
+constexpr int kPartBucket = 8 * kHeadStride;
+constexpr int kPartSum = kPartBucket + 8;
+constexpr int kPartFloats = kPartSum + 8;
 
 // Shared-memory layout of one CTA (offsets from the 1024-aligned base): per
 // worker two stages of [K 4096][V][K scales][V scales], then the mbarriers.
@@ -78,14 +85,15 @@ inline Layout layout_of(int fmt, int H, int max_workers) {
   L.ksc_off = L.v_off + L.v_bytes;
   L.vsc_off = L.ksc_off + L.ksc_bytes;
   L.stage_bytes = (L.vsc_off + L.vsc_bytes + 1023) & ~1023;
+  // a worker's partial (kPartFloats floats) goes into its own two stages
+  L.stage_bytes = std::max(L.stage_bytes, (kPartFloats * 2 + 1023) & ~1023);
   L.tx_bytes = 4096 + L.v_bytes + L.ksc_bytes + L.vsc_bytes;
-  // the merge of the epilogue reuses the stages: W x 8 heads x (256 + 2) floats
   for (L.workers = max_workers; L.workers > 1; --L.workers) {
-    L.bar_off = std::max(L.workers * 2 * L.stage_bytes, L.workers * 8 * 258 * 4);
+    L.bar_off = L.workers * 2 * L.stage_bytes;
     L.total = L.bar_off + 16 * L.workers + 16 + 1024;
     if (L.total <= kSmemCap) break;
   }
-  L.bar_off = std::max(L.workers * 2 * L.stage_bytes, L.workers * 8 * 258 * 4);
+  L.bar_off = L.workers * 2 * L.stage_bytes;
   L.total = L.bar_off + 16 * L.workers + 16 + 1024;
   return L;
 }
@@ -300,15 +308,30 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (sb - raw_s);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int W = blockDim.x >> 5;
+  const Layout& LY = p.L;
+  const uint32_t full = sb + LY.bar_off + 16 * w;                       // this worker's two stage barriers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY.bar_off + 16 * W);
+  // what needs no input of the previous kernel comes before the dependency
+  // wait: the tensor maps (kernel parameters) into the descriptor cache, and
+  // each worker's own stage barriers (its lane 0 issues that worker's copies)
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+    *abort_flag = 0;
+  }
+  if (lane == 0) {
+    mbar_init(full, 1);
+    mbar_init(full + 8, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   // launched as a programmatic dependent of the previous kernel in the stream:
   // nothing is read before it completes
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int W = blockDim.x >> 5;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const CacheView& C = p.C;
-  const Layout& LY = p.L;
   const int H = C.H, HQ = H * kGqa;
   const int r0 = lane >> 2, c = lane & 3;
 
@@ -322,21 +345,19 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   const int c_end = min(c_stop, n_vis);
   const int n_tiles = c_end > c_begin ? (c_end - c_begin + 15) >> 4 : 0;
   const int n_my = n_tiles > w ? (n_tiles - w + W - 1) / W : 0;      // tiles w + W u
-
-  const uint32_t full = sb + LY.bar_off + 16 * w;                       // this worker's two stage barriers
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY.bar_off + 16 * W);
   const uint32_t ring = sb + w * 2 * LY.stage_bytes;
 
   // ---- fused decode step: the CTA whose cells include the newest one (n_vis - 1)
   // writes the new token's K and V there before any copy of the pipeline starts
-  if (p.k_new != nullptr && w < 2) {
-    const int cell = n_vis - 1;
-    if (cell >= c_begin && cell < c_stop && p.steps[b] == n_vis) {   // skipped for a clipped length
-      const int64_t pidx = cell / C.P;
+  // (the condition is the same for the whole CTA)
+  const int new_cell = n_vis - 1;
+  if (p.k_new != nullptr && new_cell >= c_begin && new_cell < c_stop && p.steps[b] == n_vis) {   // skipped for a clipped length
+    if (w < 2) {
+      const int64_t pidx = new_cell / C.P;
       const int64_t page = pidx < p.max_pages ? p.pt[static_cast<int64_t>(b) * p.max_pages + pidx] : -1;
       if (page >= 0 && page < C.n_pages) {
         uint8_t* base = C.pages + page * C.page_bytes;
-        const int64_t r = static_cast<int64_t>(cell % C.P) * H + g;
+        const int64_t r = static_cast<int64_t>(new_cell % C.P) * H + g;
         const int64_t elem = (static_cast<int64_t>(b) * H + g) * kD + 8 * lane;
         long long* ts = reinterpret_cast<long long*>(sm) + w * kRotScratch;   // stage memory, not yet in use
         // bf16 rows take the bulk append's fast paths (same bytes, fewer
@@ -355,12 +376,66 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
       // overwrite the scratch, come after the block barrier below
       asm volatile("fence.proxy.async;" ::: "memory");
     }
+    __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * W; ++i) mbar_init(sb + LY.bar_off + 8 * i, 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+  // ---- q loads (lane: head r0, dims 64 i + 16 c + [0, 16)), issued ahead of the
+  // first copies so that they do not queue behind them; converted further down
+  constexpr int kQraw = QF32 ? 16 : 8;
+  uint4 qraw[kQraw];
+  {
+    const int64_t qrow = (static_cast<int64_t>(b) * HQ + g * kGqa + r0) * kD;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t e0 = qrow + 64 * i + 16 * c;
+      const uint4* src = QF32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(p.q) + e0)
+                              : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + e0);
+#pragma unroll
+      for (int t = 0; t < kQraw / 4; ++t) qraw[(kQraw / 4) * i + t] = src[t];
+    }
   }
+
+  // ---- this worker's copies: local tile u -> stage u & 1.  Page ids of 32
+  // consecutive local tiles are held one per lane.
+  const int32_t* pt_row = p.pt + static_cast<int64_t>(b) * p.max_pages;
+  int win0 = -1000000, win_page = -1;
+  auto page_of = [&](int u) -> int {         // warp-uniform u; all lanes call
+    if (u < win0 || u >= win0 + 32) {
+      win0 = u;
+      const int cell = c_begin + 16 * (w + W * (u + lane));
+      const int64_t pidx = cell >= 0 ? static_cast<int64_t>(p.page_div.div(static_cast<uint32_t>(cell))) : 0;
+      win_page = (u + lane < n_my && pidx < p.max_pages) ? pt_row[pidx] : -1;
+    }
+    const int page = __shfl_sync(kFull, win_page, u - win0);
+    return (page >= 0 && page < C.n_pages) ? page : -1;
+  };
+  // an out-of-range page id issues no copy (the stage barrier is completed by a
+  // plain arrive) and is recorded; the tile is then skipped
+  auto issue = [&](int u, int page) {
+    if (lane == 0) {
+      const uint32_t st = ring + (u & 1) * LY.stage_bytes;
+      const uint32_t bar = full + 8 * (u & 1);
+      if (page >= 0) {
+        const int cell0 = c_begin + 16 * (w + W * u);
+        const int slot0 = cell0 - static_cast<int>(p.page_div.div(static_cast<uint32_t>(cell0))) * C.P;
+        mbar_expect_tx(bar, LY.tx_bytes);
+        tma_load_4d(st, &tm_k, 0, g, slot0, page, bar);
+        tma_load_4d(st + 2048, &tm_k, 128, g, slot0, page, bar);
+        tma_load_4d(st + LY.v_off, &tm_v, 0, g, slot0, page, bar);
+        if (kI8) tma_load_4d(st + LY.v_off + 2048, &tm_v, 128, g, slot0, page, bar);
+        const uint8_t* pg = C.pages + static_cast<int64_t>(page) * C.page_bytes;
+        bulk_load(st + LY.ksc_off, pg + C.ks_off() + static_cast<int64_t>(slot0) * 8 * H, LY.ksc_bytes, bar);
+        bulk_load(st + LY.vsc_off, pg + C.vs_off() + static_cast<int64_t>(slot0) * (kI8 ? 8 : 16) * H,
+                  LY.vsc_bytes, bar);
+      } else {
+        record_status(p.status, K8V4_ERANGE);
+        mbar_arrive(bar);
+      }
+    }
+  };
+  // the first two copies go out before the q set-up, whose loads overlap them
+  int issued = 0;
+  for (; issued < min(2, n_my); ++issued) issue(issued, page_of(issued));
 
   // ---- q fragments (B operand of S^T = K q^T): lane holds head r0, dims
   // 64 i + 16 c + 4 j + e of k-step 4 i + j
@@ -368,24 +443,20 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   uint32_t qf_lo[QF32 ? 16 : 1][2];
   float f0, f1;                        // score factors of heads 2c, 2c+1
   {
-    const int64_t qrow = (static_cast<int64_t>(b) * HQ + g * kGqa + r0) * kD;
     float qv[64];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int64_t e0 = qrow + 64 * i + 16 * c;
       if (QF32) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + e0);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const float4 v4 = src[t];
-          qv[16 * i + 4 * t] = v4.x; qv[16 * i + 4 * t + 1] = v4.y;
-          qv[16 * i + 4 * t + 2] = v4.z; qv[16 * i + 4 * t + 3] = v4.w;
+          const uint4 raw = qraw[4 * i + t];
+          qv[16 * i + 4 * t] = __uint_as_float(raw.x); qv[16 * i + 4 * t + 1] = __uint_as_float(raw.y);
+          qv[16 * i + 4 * t + 2] = __uint_as_float(raw.z); qv[16 * i + 4 * t + 3] = __uint_as_float(raw.w);
         }
       } else {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + e0);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const uint4 raw = src[t];
+          const uint4 raw = qraw[2 * i + t];
           const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -429,51 +500,6 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   }
   __syncthreads();
 
-  // ---- this worker's copies: local tile u -> stage u & 1.  Page ids of 32
-  // consecutive local tiles are held one per lane.
-  const int32_t* pt_row = p.pt + static_cast<int64_t>(b) * p.max_pages;
-  int win0 = -1000000, win_page = -1;
-  auto page_of = [&](int u) -> int {         // warp-uniform u; all lanes call
-    if (u < win0 || u >= win0 + 32) {
-      win0 = u;
-      const int cell = c_begin + 16 * (w + W * (u + lane));
-      const int64_t pidx = cell >= 0 ? static_cast<int64_t>(p.page_div.div(static_cast<uint32_t>(cell))) : 0;
-      win_page = (u + lane < n_my && pidx < p.max_pages) ? pt_row[pidx] : -1;
-    }
-    const int page = __shfl_sync(kFull, win_page, u - win0);
-    return (page >= 0 && page < C.n_pages) ? page : -1;
-  };
-  // an out-of-range page id issues no copy (the stage barrier is completed by a
-  // plain arrive) and is recorded; the tile is then skipped
-  auto issue = [&](int u, int page) {
-    if (lane == 0) {
-      const uint32_t st = ring + (u & 1) * LY.stage_bytes;
-      const uint32_t bar = full + 8 * (u & 1);
-      if (page >= 0) {
-        const int cell0 = c_begin + 16 * (w + W * u);
-        const int slot0 = cell0 - static_cast<int>(p.page_div.div(static_cast<uint32_t>(cell0))) * C.P;
-        mbar_expect_tx(bar, LY.tx_bytes);
-        tma_load_4d(st, &tm_k, 0, g, slot0, page, bar);
-        tma_load_4d(st + 2048, &tm_k, 128, g, slot0, page, bar);
-        tma_load_4d(st + LY.v_off, &tm_v, 0, g, slot0, page, bar);
-        if (kI8) tma_load_4d(st + LY.v_off + 2048, &tm_v, 128, g, slot0, page, bar);
-        const uint8_t* pg = C.pages + static_cast<int64_t>(page) * C.page_bytes;
-        bulk_load(st + LY.ksc_off, pg + C.ks_off() + static_cast<int64_t>(slot0) * 8 * H, LY.ksc_bytes, bar);
-        bulk_load(st + LY.vsc_off, pg + C.vs_off() + static_cast<int64_t>(slot0) * (kI8 ? 8 : 16) * H,
-                  LY.vsc_bytes, bar);
-      } else {
-        record_status(p.status, K8V4_ERANGE);
-        mbar_arrive(bar);
-      }
-    }
-  };
-  if (lane == 0 && n_my > 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
-  }
-  int issued = 0;
-  for (; issued < min(2, n_my); ++issued) issue(issued, page_of(issued));
-
   // K fragment addresses within a stage (two 128-byte-swizzled [16][128] halves)
   const int rowA = sigma(r0), rowB = 8 + sigma(r0);
   uint32_t offA[4], offB[4];
@@ -502,6 +528,7 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   int M0 = INT_MIN, M1 = INT_MIN;      // running buckets of heads 2c, 2c+1
   float l0 = 0.0f, l1 = 0.0f;          // this lane's share of the sums of p' (heads 2c, 2c+1)
   const uint32_t wait_ns = p.wait_ns;
+  bool aborted = false;                // this warp left the loop with copies in flight
 
   for (int u = 0; u < n_my; ++u) {
     const int s = u & 1;
@@ -510,6 +537,7 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
         *abort_flag = 1;
         record_status(p.status, K8V4_ECUDA);
       }
+      aborted = true;
       break;
     }
     const uint32_t st = ring + s * LY.stage_bytes;
@@ -675,53 +703,60 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   }
 
   // ---------------------------------------------------------------- epilogue
-  __syncthreads();
-  if (*abort_flag) {
-    // copies still in flight land before the stage memory is reused: wait
-    // (bounded) for the last fill of each stage this warp issued
-    if (lane == 0) {
-      for (int u = max(0, issued - 2); u < issued; ++u) {
-        const uint64_t t0 = global_ns();
-        while (!mbar_try_sleep(full + 8 * (u & 1), (u >> 1) & 1, 20000u) && global_ns() - t0 < kWaitDefaultNs) {
-        }
+  // Each worker writes its partial (kPartFloats: o by rotated dim, buckets,
+  // sums) into its own two stages as soon as its loop ends, while the others
+  // may still stream.  A worker that left the loop early first waits (bounded)
+  // for its copies still in flight.  A head with nothing visible writes zeros,
+  // so the merge below needs no test.
+  if (aborted && lane == 0) {
+    for (int u = max(0, issued - 2); u < issued; ++u) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_sleep(full + 8 * (u & 1), (u >> 1) & 1, 20000u) && global_ns() - t0 < kWaitDefaultNs) {
       }
     }
-    __syncthreads();
   }
-  // each worker's partial: [8 heads][256] floats, then 8 buckets and 8 sums
-  float* mine = reinterpret_cast<float*>(sm) + w * 8 * 258;
+  __syncwarp();
+  float* mine = reinterpret_cast<float*>(sm + w * 2 * LY.stage_bytes);
+  const bool live0 = M0 != INT_MIN, live1 = M1 != INT_MIN;
 #pragma unroll
   for (int mt = 0; mt < kMT; ++mt) {
     const int d0 = kI8 ? 16 * mt + 2 * r0 : 32 * (mt >> 1) + 16 * (mt & 1) + 2 * r0;
-    *reinterpret_cast<float2*>(mine + (2 * c) * 256 + d0) = make_float2(o[mt][0], o[mt][2]);
-    *reinterpret_cast<float2*>(mine + (2 * c + 1) * 256 + d0) = make_float2(o[mt][1], o[mt][3]);
+    *reinterpret_cast<float2*>(mine + (2 * c) * kHeadStride + d0) =
+        live0 ? make_float2(o[mt][0], o[mt][2]) : make_float2(0.0f, 0.0f);
+    *reinterpret_cast<float2*>(mine + (2 * c + 1) * kHeadStride + d0) =
+        live1 ? make_float2(o[mt][1], o[mt][3]) : make_float2(0.0f, 0.0f);
   }
   if (r0 == 0) {
-    reinterpret_cast<int*>(mine + 2048)[2 * c] = M0;
-    reinterpret_cast<int*>(mine + 2048)[2 * c + 1] = M1;
-    mine[2056 + 2 * c] = l0;
-    mine[2056 + 2 * c + 1] = l1;
+    reinterpret_cast<int*>(mine + kPartBucket)[2 * c] = M0;
+    reinterpret_cast<int*>(mine + kPartBucket)[2 * c + 1] = M1;
+    mine[kPartSum + 2 * c] = l0;
+    mine[kPartSum + 2 * c + 1] = l1;
   }
   __syncthreads();
-  // one warp per head: merge the workers' partials at the largest bucket, bring
-  // the row back from rotated space and write (o, m, l)
+  // one warp per head: merge the workers' partials at the largest bucket (lane
+  // j reads worker j's bucket and sum), bring the row back from rotated space
+  // and write (o, m, l).  The lane holds dims 4 lane + e and 128 + 4 lane + e
+  // (e < 4) as v[e] and v[4 + e], so every shared-memory read is conflict free.
   for (int h = w; h < kGqa; h += W) {
-    const float* part = reinterpret_cast<const float*>(sm);
-    int Mx = INT_MIN;
-    for (int j = 0; j < W; ++j) Mx = max(Mx, reinterpret_cast<const int*>(part + j * 8 * 258 + 2048)[h]);
+    const float* mj_part = reinterpret_cast<const float*>(sm + min(lane, W - 1) * 2 * LY.stage_bytes);
+    const int mj = lane < W ? reinterpret_cast<const int*>(mj_part + kPartBucket)[h] : INT_MIN;
+    const float lj = lane < W ? mj_part[kPartSum + h] : 0.0f;
+    int Mx = mj;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) Mx = max(Mx, __shfl_xor_sync(kFull, Mx, off));
+    const float fj = mj == INT_MIN ? 0.0f : pow2i(8 * (mj - Mx));
     float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
     float L = 0.0f;
-    if (Mx != INT_MIN) {
-      for (int j = 0; j < W; ++j) {
-        const float* src = part + j * 8 * 258;
-        const int mj = reinterpret_cast<const int*>(src + 2048)[h];
-        if (mj == INT_MIN) continue;
-        const float sc2 = pow2i(8 * (mj - Mx));
-        const float4 x0 = *reinterpret_cast<const float4*>(src + h * 256 + 8 * lane);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + h * 256 + 8 * lane + 4);
-        v[0] += x0.x * sc2; v[1] += x0.y * sc2; v[2] += x0.z * sc2; v[3] += x0.w * sc2;
-        v[4] += x1.x * sc2; v[5] += x1.y * sc2; v[6] += x1.z * sc2; v[7] += x1.w * sc2;
-        L += src[2056 + h] * sc2;
+#pragma unroll
+    for (int j = 0; j < (QF32 ? kMaxWorkersF32 : kMaxWorkers); ++j) {
+      const float f = __shfl_sync(kFull, fj, j), lw = __shfl_sync(kFull, lj, j);   // 0 for j >= W
+      if (j < W) {
+        const float* src = reinterpret_cast<const float*>(sm + j * 2 * LY.stage_bytes) + h * kHeadStride;
+        const float4 x0 = *reinterpret_cast<const float4*>(src + 4 * lane);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + 128 + 4 * lane);
+        v[0] += x0.x * f; v[1] += x0.y * f; v[2] += x0.z * f; v[3] += x0.w * f;
+        v[4] += x1.x * f; v[5] += x1.y * f; v[6] += x1.z * f; v[7] += x1.w * f;
+        L += lw * f;
       }
     }
     float scale;
@@ -750,8 +785,8 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
       scale = 1.0f / 16384.0f;          // 2^-14 of p'
     }
     float* dst = p.ws + ((static_cast<int64_t>(b) * p.splits + split) * HQ + g * kGqa + h) * kPStride;
-    reinterpret_cast<float4*>(dst + 8 * lane)[0] = make_float4(v[0] * scale, v[1] * scale, v[2] * scale, v[3] * scale);
-    reinterpret_cast<float4*>(dst + 8 * lane)[1] = make_float4(v[4] * scale, v[5] * scale, v[6] * scale, v[7] * scale);
+    reinterpret_cast<float4*>(dst)[lane] = make_float4(v[0] * scale, v[1] * scale, v[2] * scale, v[3] * scale);
+    reinterpret_cast<float4*>(dst)[32 + lane] = make_float4(v[4] * scale, v[5] * scale, v[6] * scale, v[7] * scale);
     if (lane == 0) {
       dst[256] = Mx == INT_MIN ? -INFINITY : static_cast<float>(8 * Mx);
       dst[257] = L * (1.0f / 16384.0f);

@@ -6,12 +6,14 @@
 // of a cell-range split hands to the others.
 //
 // One CTA per (row, 32-dim chunk), eight warps.  Warp w takes splits w, w + 8,
-// ... in rounds of kRound: every load of a round (each split's m and l, and the
+// ... in rounds of R: every load of a round (each split's m and l, and the
 // lane's element of o) is issued before any is used, so a round costs one L2
 // round trip; the round is folded at its own maximum into the warp's running
-// (M, L, acc), and the eight warp states are merged in shared memory.  A long
-// single-sequence decode (76 splits per KV head on 152 SMs) takes one round;
-// 12 splits of a warp fit 64 registers, four CTAs per SM.  Launched as a programmatic
+// (M, L, acc), and the eight warp states are merged in shared memory.  Two
+// instantiations: R = 12 (64 registers, four CTAs per SM) for many splits, so
+// that a long single-sequence decode (76 splits per KV head on 152 SMs) takes
+// one round; R = 3 (32 registers, eight CTAs per SM) for up to 24 splits, where
+// a batch of sequences brings thousands of rows.  Launched as a programmatic
 // dependent of the split kernel: the launch overlaps the split kernel's tail and
 // griddepcontrol.wait holds the loads until the partials are written.
 #include "k8v4_common.cuh"
@@ -20,13 +22,15 @@ namespace k8v4 {
 namespace {
 
 constexpr int kPStride = 260;   // floats per partial row: o[256], m, l, 2 pad
-constexpr int kRound = 12;      // splits per warp whose loads are in flight together
+constexpr int kRoundMany = 12;  // splits per warp whose loads are in flight together
+constexpr int kRoundFew = 3;
 
 // row r = (b, rr) with rr < rows_per_b; split s of row r at
 // src + b * b_stride + s * split_stride + rr * kPStride
-__global__ void __launch_bounds__(256, 4) combine_kernel(const float* __restrict__ src, int splits, int64_t split_stride,
-                                                      int64_t b_stride, int rows_per_b, float* __restrict__ out,
-                                                      int write_partial) {
+template <int R>
+__global__ void __launch_bounds__(256, R <= kRoundFew ? 8 : 4)
+    combine_kernel(const float* __restrict__ src, int splits, int64_t split_stride, int64_t b_stride, int rows_per_b,
+                   float* __restrict__ out, int write_partial) {
   __shared__ float wm[8], wl[8], wacc[8][32];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -35,10 +39,10 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(const float* __restrict
   const float* base = src + b * b_stride + static_cast<int64_t>(rr) * kPStride;
   const int dim = chunk * 32 + lane;
   float M = -INFINITY, L = 0.0f, acc = 0.0f;
-  for (int s0 = warp; s0 < splits; s0 += 8 * kRound) {
-    float ms[kRound], ls[kRound], xs[kRound];
+  for (int s0 = warp; s0 < splits; s0 += 8 * R) {
+    float ms[R], ls[R], xs[R];
 #pragma unroll
-    for (int k = 0; k < kRound; ++k) {
+    for (int k = 0; k < R; ++k) {
       const int s = s0 + 8 * k;
       ms[k] = -INFINITY;
       ls[k] = xs[k] = 0.0f;
@@ -51,13 +55,13 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(const float* __restrict
     }
     float mr = M;
 #pragma unroll
-    for (int k = 0; k < kRound; ++k) mr = fmaxf(mr, ms[k]);
+    for (int k = 0; k < R; ++k) mr = fmaxf(mr, ms[k]);
     if (mr == -INFINITY) continue;                      // nothing visible yet (the same for the warp)
     const float a = exp2f(M - mr);                      // 0 while M = -inf
     acc *= a;
     L *= a;
 #pragma unroll
-    for (int k = 0; k < kRound; ++k) {
+    for (int k = 0; k < R; ++k) {
       if (ms[k] == -INFINITY) continue;                 // a split with nothing visible
       const float wk = exp2f(ms[k] - mr);
       acc += xs[k] * wk;
@@ -113,9 +117,13 @@ int launch(const Launch& L, const float* src, int splits, int64_t split_stride, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel, src, splits, split_stride, b_stride, rows_per_b, out, write_partial) !=
-      cudaSuccess)
-    return K8V4_ECUDA;
+  const cudaError_t e =
+      splits <= 8 * kRoundFew
+          ? cudaLaunchKernelEx(&cfg, combine_kernel<kRoundFew>, src, splits, split_stride, b_stride, rows_per_b, out,
+                               write_partial)
+          : cudaLaunchKernelEx(&cfg, combine_kernel<kRoundMany>, src, splits, split_stride, b_stride, rows_per_b, out,
+                               write_partial);
+  if (e != cudaSuccess) return K8V4_ECUDA;
   return cudaGetLastError() == cudaSuccess ? K8V4_OK : K8V4_ECUDA;
 }
 

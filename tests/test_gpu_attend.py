@@ -269,3 +269,36 @@ def test_other_kv_head_counts(fmt, H):
     rs, rh, rv = oracle.multi_query_rows(steps, HQ)
     qrows = np.concatenate([x.f32.reshape(-1, 256) for x in qs])
     assert rel_err(got.reshape(-1, 256), ref.attention(pt, rs, rh, rv, qrows)) <= TOL
+
+
+def test_one_kv_head_long_sequence_many_splits():
+    """One KV head (8 query heads) and one 65,536-cell sequence: decode cuts it
+    into more than 96 cell ranges and verify into more still, so the combine's
+    many-split instantiation folds each warp's splits over several rounds (12
+    splits a round), rescaling its running sum at each new round maximum.  All
+    decode rows and a 5-query verify window against the oracle."""
+    n, H, P = 65536, 1, 64
+    seed = synth.config_seed(3) + 211
+    n_pages = n // P
+    k = synth.kv_values(seed, synth.T_K, 0, n, H, 3, "bf16")
+    v = synth.kv_values(seed, synth.T_V, 0, n, H, 3, "bf16")
+    pt = synth.page_table_shuffled(seed, synth.stream_id(synth.T_PT, 0), n_pages, n_pages).reshape(1, -1)
+    gpu, ref = make_caches(n_pages, P, H)
+    pt_d = append_both(gpu, ref, pt, np.array([0]), synth.Tensor(k.f32[None], "bf16"), synth.Tensor(v.f32[None], "bf16"))
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    row_bytes = 8 * H * 1040                    # one partial row (260 floats) per query head
+    assert k8.attn_k8v4_workspace_bytes(gpu, 1, 1, n) // row_bytes > 96
+    assert k8.attn_k8v4_workspace_bytes(gpu, 1, 5, n) // (5 * row_bytes) > 96
+    lens = np.array([n], np.int32)
+    q = synth.q_values(seed, 0, 1, H, "bf16")
+    got = decode_gpu(gpu, dev_tensor(q, (1, 8, 256)), pt_d, lens, n)
+    assert k8.k8v4_last_device_status() == 0
+    rs, rh, rv = oracle.decode_rows(1, 8, lens)
+    assert rel_err(got.reshape(-1, 256), ref.attention(pt, rs, rh, rv, q.f32.reshape(-1, 256))) <= TOL
+    steps = (n - 4 + np.arange(5)).astype(np.int32)[None]
+    qv = synth.q_values(seed, 1, 5, H, "bf16")
+    got = verify_gpu(gpu, dev_tensor(qv)[None], pt_d, steps, n)
+    assert k8.k8v4_last_device_status() == 0
+    rs, rh, rv = oracle.multi_query_rows(steps, 8)
+    assert rel_err(got.reshape(-1, 256), ref.attention(pt, rs, rh, rv, qv.f32.reshape(-1, 256))) <= TOL

@@ -15,8 +15,9 @@
  *
  * Conventions for every call:
  *  - All array arguments are DEVICE pointers owned by the caller (the library
- *    never allocates; scratch lives in the caller's workspace).  `stream` is a
- *    cudaStream_t (NULL = legacy default stream).  Calls are asynchronous.
+ *    never allocates; scratch lives in the caller's workspace), except where
+ *    a call allows page-locked host memory.  `stream` is a cudaStream_t
+ *    (NULL = legacy default stream).  Calls are asynchronous.
  *  - Arguments are validated on the host before any launch; a call that fails
  *    validation launches nothing and returns a negative k8v4_status.
  *  - Values that live in device memory (positions, lengths, page-table entries)
@@ -145,6 +146,11 @@ size_t attn_k8v4_workspace_bytes(const k8v4_cache* cache, int32_t n_seqs, int32_
  *   out:      float [n_seqs][8*H][256], the un-rotated attention output.
  *   workspace: >= attn_k8v4_workspace_bytes(cache, n_seqs, 1, max_seq_len)
  *             bytes of device memory, 256-byte aligned.
+ * q and out may instead be page-locked host memory that the device addresses
+ * directly (cudaHostAlloc, or cudaHostRegister with mapping, under unified
+ * addressing): the kernels read q and write out with plain loads and stores
+ * across the host link, so a serving loop needs no copy launches of its own;
+ * out is complete when the stream reaches the end of the call.
  * A row with zero visible cells outputs zeros.  Works on every format. */
 int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                      int64_t max_pages, const int32_t* seq_lens, int32_t n_seqs, int32_t max_seq_len,
@@ -159,7 +165,8 @@ int attn_k8v4_decode(const k8v4_cache* cache, const void* q, int32_t q_dtype, co
  * split-K grid whose cell range holds the newest cell writes it before any of
  * its warps reads that cell, so the append costs no separate launch.
  *   k_new, v_new: [n_seqs][H][256] of kv_dtype (K8V4_F32 or K8V4_BF16),
- *             16-byte aligned, device memory.
+ *             16-byte aligned; device memory, or page-locked host memory as
+ *             q and out (read with plain loads by the CTA that appends).
  *   seq_lens: int32 [n_seqs] (device), each in [1, max_seq_len] for a sequence
  *             that gets a token (0: no token, zero output); a length past
  *             max_seq_len is clipped, recorded, and its token not written.

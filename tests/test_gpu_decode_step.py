@@ -146,3 +146,39 @@ def test_decode_step_many_sequences():
     rs, rh, rv = oracle.decode_rows(n, 16, lens)
     want = ref.attention(pt, rs, rh, rv, q.f32.reshape(-1, 256))
     assert rel_err(out.cpu().numpy().reshape(-1, 256), want) <= TOL
+
+
+@pytest.mark.parametrize("fmt,kvdt", [(k8.FORMAT_K8V4, "bf16"), (k8.FORMAT_INT8, "bf16"), (k8.FORMAT_Q4, "f32")])
+def test_decode_step_host_buffers_equal_device_buffers(fmt, kvdt):
+    """q, the new rows and the output may live in page-locked host memory: the
+    kernels read and write them over the host link.  Same cache bytes and the
+    same output, bit for bit, as with device buffers, for the fused step and the
+    plain decode."""
+    lens = [1, 17, 1000, 5000, 0, 4097]
+    pt, lens, q, gpu_a, gpu_b, ref, k_new, v_new = _setup(fmt, kvdt, lens, seed_off=7)
+    n = len(lens)
+    max_len = int(lens.max())
+    pt_d = torch.from_numpy(pt).cuda()
+    lens_d = torch.from_numpy(lens).cuda()
+    qd = dev_tensor(q, (n, 16, 256))
+    kd, vd = dev_tensor(k_new, (n, 2, 256)), dev_tensor(v_new, (n, 2, 256))
+    qh, kh, vh = qd.cpu().pin_memory(), kd.cpu().pin_memory(), vd.cpu().pin_memory()
+    ws = k8.workspace(gpu_a, n, 1, max_len)
+    out_d = torch.empty(n, 16, 256, dtype=torch.float32, device="cuda")
+    out_h = torch.full((n, 16, 256), float("nan"), dtype=torch.float32).pin_memory()
+    k8.attn_k8v4_decode_step(gpu_a, qd, kd, vd, pt_d, lens_d, max_len, out_d, ws)
+    k8.attn_k8v4_decode_step(gpu_b, qh, kh, vh, pt_d, lens_d, max_len, out_h, ws)
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    assert torch.equal(gpu_a.pages, gpu_b.pages)
+    assert np.array_equal(gpu_b.pages.cpu().numpy(), ref.buf)
+    assert torch.equal(out_d.cpu(), out_h)
+    rs, rh, rv = oracle.decode_rows(n, 16, lens)
+    want = ref.attention(pt, rs, rh, rv, q.f32.reshape(-1, 256))
+    assert rel_err(out_h.numpy().reshape(-1, 256), want) <= TOL
+    out_h.fill_(float("nan"))
+    k8.attn_k8v4_decode(gpu_b, qh, pt_d, lens_d, max_len, out_h, ws)
+    k8.attn_k8v4_decode(gpu_b, qd, pt_d, lens_d, max_len, out_d, ws)
+    torch.cuda.synchronize()
+    assert k8.k8v4_last_device_status() == 0
+    assert torch.equal(out_d.cpu(), out_h)

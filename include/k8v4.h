@@ -202,8 +202,8 @@ int attn_k8v4_decode_noalloc(const k8v4_cache* cache, const void* q, int32_t q_d
 
 /* ---------------------------------------------------------------- split across GPUs
  * One long sequence's decode split by cell range over several GPUs (the path
- * the k8v4 PR's engine runs with its multi-GPU split, header: "Rebased on
- * v0.1.21 (the multi-GPU layer split)"): GPU r attends over its cells
+ * the k8v4 PR's engine runs with its multi-GPU split: the PR's header says it
+ * sits on the engine release that splits layers across GPUs): GPU r attends over its cells
  * [cell_begin_r, cell_end_r) with attn_k8v4_decode_partial, the partial rows of
  * all GPUs are exchanged (an all-gather of n_seqs * 8H * 260 floats per GPU),
  * and every GPU merges them with attn_k8v4_combine_partials.  The merged result

@@ -4,9 +4,10 @@ TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers.  The CUDA library never imports it.
 
 Every function restates the cache's arithmetic as described by the hybrid
-"--kv k8v4" pull request ("What": INT8 K, Hadamard-rotated Q4_0 V, 816 B/cell;
-"Tests": INT8 rules with ties-to-even, rotated q4_0 rules, host attention over
-the dequantised K/V) with the readings listed at the top of k8v4_oracle.c.
+k8v4 pull request (What section: K as INT8 and V rotated by a Hadamard
+transform and stored as Q4_0, 816 B per cell; Tests section: int8 codes round
+half to even, the rotated q4_0 rules, attention on the host over the
+dequantised K and V) with the readings listed at the top of k8v4_oracle.c.
 """
 from __future__ import annotations
 

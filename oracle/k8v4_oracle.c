@@ -12,10 +12,10 @@
  * Readings where the pages are silent (each also listed in the design notes):
  *  - K: symmetric int8, one fp32 scale per 128-lane half, s = absmax / 127
  *    (IEEE fp32 division), code = clamp(rint_even(x / s), -127, 127); s == 0 gives
- *    all-zero codes.  ("INT8 rules with ties-to-even", Tests section.)
+ *    all-zero codes.  (Tests section: int8 codes round half to even.)
  *  - V rotation: y_i = RN_fp32( (sum_j H[i][j] x_j) / 16 ), H the Sylvester
  *    Hadamard matrix H[i][j] = (-1)^popcount(i & j), the sum taken EXACTLY (a
- *    multi-limb integer) and rounded once.  ("rotated q4_0", What section.)
+ *    multi-limb integer) and rounded once.  (What section: V is stored as rotated q4_0.)
  *  - V Q4_0 per 32-lane block: m = the element of largest |y| (first index on
  *    ties), d = fp16_RN(m / -8) (fp32 division, then one rounding to fp16),
  *    code = clamp(rint_even(y / (float)d) + 8, 0, 15); d == 0 gives codes 8.

@@ -1,8 +1,9 @@
 """Write int8_quotient.txt and q4_quotient.txt: quantiser inputs whose codes
 depend on HOW the quotient is rounded.
 
-The k8v4 PR ("Tests": "INT8 rules with ties-to-even"; "What": V as rotated
-q4_0) fixes the rounding of the code but not the arithmetic of the quotient.
+The k8v4 PR (Tests section: int8 codes round half to even; What section: V
+stored as rotated q4_0) fixes the rounding of the code but not the arithmetic
+of the quotient.
 This library reads it as ONE IEEE fp32 division, x / s (int8 K) and y / d
 (q4_0 V), each correctly rounded, then rint ties-to-even.  Two plausible
 alternatives give different codes on some inputs:

@@ -209,7 +209,7 @@ def _read_quotient_golden(name):
 
 def test_int8_quotient_is_one_ieee_division(orc):
     """Codes that tell x / s apart from x * (1 / s) and from (x * 127) / a (the
-    PR's "INT8 rules with ties-to-even" fix the rounding of the code; the
+    PR's Tests section fixes the rounding of the code, half to even; the
     quotient is read as one correctly rounded fp32 division).  Each fixture line
     was derived with exact rational arithmetic; a non-power-of-two absmax makes
     the three readings differ."""
@@ -315,7 +315,8 @@ def test_q4_error_bounds(orc):
 def test_bytes_per_cell(orc):
     assert 2 * orc.bytes_per_cell_head(orc.FMT_K8V4) == 816
     assert 2 * orc.bytes_per_cell_head(orc.FMT_INT8) == 1056
-    # "816 B per cell vs int8's 1,056 (-23%) and q4_0's 576" (#120, section "What")
+    # the k8v4 PR (#120, section "What") gives 816 B per cell against 1,056 for
+    # all-int8 and 576 for all-q4_0
     assert 2 * orc.bytes_per_cell_head(orc.FMT_Q4) == 576
     # 816 = 512 K codes + 16 K scales + 256 V nibbles + 32 V scales
     assert 2 * (256 + 8 + 128 + 16) == 816

@@ -139,6 +139,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   }
   __syncthreads();
   if (part == 0 && my_vis > 0) atomicMax(nmax_s, my_vis);
+  __syncthreads();
+  // a split past every row's visible cells (a short sequence of a verify batch)
+  // only marks its partial rows empty (m = -inf: the combine skips them) and
+  // leaves before tensor memory, Q and the pipeline are set up
+  if (p.ws && split * p.cells_per_split >= *nmax_s) {
+    for (int r = tid; r < kRows; r += kThreads) {
+      const int t = tok0 + r / kGqa, h = r % kGqa;
+      if (t >= p.n_q_tok) continue;
+      float* dst = p.ws + ((((static_cast<int64_t>(b) * p.splits + split) * p.n_q_tok + t) * HQ) + g * kGqa + h) * 260;
+      dst[256] = -INFINITY;
+      dst[257] = 0.0f;
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;
+  }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
 
   // ---- Q rows -> fp16 with a per-row power-of-two scale, swizzled K-major;

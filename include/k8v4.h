@@ -341,6 +341,17 @@ int kv_stream_copy(const k8v4_cache* host, const k8v4_cache* dev, const int32_t*
  * the recovery path is tested.  Process-wide; not for production use. */
 void k8v4_set_wait_limit_ns(uint32_t ns);
 
+/* Failure-handling diagnostics: nonzero makes every later launch of the
+ * TMA-fed decode kernel (attn_k8v4_decode, _decode_step, _decode_noalloc and
+ * _decode_partial on the K8V4 and INT8 formats) withhold the copies of one
+ * tile: worker 0 of the CTA for split 0, KV head 0, sequence 0 never issues
+ * its first tile, so its wait on that stage runs out after the wait bound
+ * (k8v4_set_wait_limit_ns) -- a phase that nothing completes -- and the kernel
+ * records K8V4_ECUDA, closes that stage itself, waits for its copies in flight
+ * and returns.  Zero restores normal operation.  Process-wide; not for
+ * production use. */
+void k8v4_set_withheld_copy(int32_t on);
+
 /* Synchronise `stream`, return the first device-side error recorded since the
  * last call (K8V4_OK if none) and clear it.  The word is per device and shared
  * by all streams. */

@@ -73,6 +73,7 @@ def lib():
             "attn_k8v4_decode_partial": ([C, P, I32, P, I64, P, I32, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
             "attn_k8v4_combine_partials": ([P, I32, I32, I32, P, P], ctypes.c_int),
             "k8v4_set_wait_limit_ns": ([ctypes.c_uint32], None),
+            "k8v4_set_withheld_copy": ([ctypes.c_int32], None),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(L, name)
@@ -89,7 +90,7 @@ EXPORTED = ("k8v4_bytes_per_cell", "k8v4_status_string", "k8v4_device_check", "k
             "kv_dequant_k8v4", "k8v4_last_device_status",
             "kv_append_k8v4_mirrored", "kv_stream_workspace_bytes", "kv_stream_resolve", "kv_stream_copy",
             "attn_k8v4_partial_workspace_bytes", "attn_k8v4_decode_partial", "attn_k8v4_combine_partials",
-            "k8v4_set_wait_limit_ns")
+            "k8v4_set_wait_limit_ns", "k8v4_set_withheld_copy")
 
 
 def status_string(code: int) -> str:
@@ -356,3 +357,8 @@ def gather_partials(part: torch.Tensor, group=None) -> torch.Tensor:
 def k8v4_set_wait_limit_ns(ns: int) -> None:
     """Failure-handling diagnostics: bound of every mbarrier wait (0: default)."""
     lib().k8v4_set_wait_limit_ns(int(ns))
+
+
+def k8v4_set_withheld_copy(on: bool) -> None:
+    """Failure-handling diagnostics: the TMA decode kernel withholds one tile's copies."""
+    lib().k8v4_set_withheld_copy(1 if on else 0)

@@ -23,6 +23,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint32_t> g_wait_ns{0};       // 0: each kernel's default bound
+std::atomic<int> g_withhold{0};           // diagnostics: the TMA decode kernel withholds one copy
 
 // Per-device set-up, done once with the device current: check that it is an
 // sm_103 part and find the device address of the status word.
@@ -114,6 +115,7 @@ int mirror_address(const k8v4_cache* host, CacheView* M) {
 }  // namespace
 
 uint32_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int withheld_copy() { return g_withhold.load(std::memory_order_relaxed); }
 
 }  // namespace k8v4
 
@@ -270,6 +272,8 @@ int attn_k8v4_combine_partials(const float* parts, int32_t n_parts, int32_t n_se
 }
 
 void k8v4_set_wait_limit_ns(uint32_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
+
+void k8v4_set_withheld_copy(int32_t on) { g_withhold.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 int attn_k8v4_prefill(const k8v4_cache* cache, const void* q, int32_t q_dtype, const int32_t* page_table,
                       int64_t max_pages, int32_t seq_len, int32_t n_q_tok, const int32_t* step_arrays, float sm_scale,

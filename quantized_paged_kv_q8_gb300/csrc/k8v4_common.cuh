@@ -160,6 +160,8 @@ int launch_verify_ws(const Launch& L, const CacheView& C, const void* q, const i
                      const int32_t* steps, int n_seqs, int n_q, int max_seq_len, float sm_scale, float* out, void* ws);
 // the bound of the mbarrier waits in the tensor-memory and TMA kernels (ns; 0: default)
 uint32_t wait_limit_ns();
+// diagnostics: nonzero makes the TMA decode kernel withhold its first CTA's first copy
+int withheld_copy();
 // weighted sum of split partials (o[256], m, l rows of 260 floats) -> out, launched programmatically dependent
 int launch_combine(const Launch& L, const float* ws, int splits, int n_seqs, int n_q, int H, float* out);
 // the splits of a one-query decode merged into one unnormalised partial row per (sequence, query head)

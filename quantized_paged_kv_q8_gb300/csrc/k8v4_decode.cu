@@ -113,6 +113,7 @@ struct DecodeParams {
   const void* v_new;
   int kv_bf16;
   uint32_t wait_ns;       // bound of every mbarrier wait, nanoseconds
+  int withhold;           // diagnostics: worker 0 of CTA (0, 0, 0) never issues its tile 0
   FastDiv page_div;       // division by the page size P
   Layout L;
 };
@@ -346,6 +347,18 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   const int n_tiles = c_end > c_begin ? (c_end - c_begin + 15) >> 4 : 0;
   const int n_my = n_tiles > w ? (n_tiles - w + W - 1) / W : 0;      // tiles w + W u
   const uint32_t ring = sb + w * 2 * LY.stage_bytes;
+  // a cell range past the sequence's visible cells (a short sequence of a
+  // ragged batch; never the range holding a new token) only marks its partial
+  // rows empty (m = -inf: the combine skips them) and leaves
+  if (n_tiles == 0) {
+    if (threadIdx.x < kGqa) {
+      float* dst = p.ws + ((static_cast<int64_t>(b) * p.splits + split) * HQ + g * kGqa + threadIdx.x) * kPStride;
+      dst[256] = -INFINITY;
+      dst[257] = 0.0f;
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;
+  }
 
   // ---- fused decode step: the CTA whose cells include the newest one (n_vis - 1)
   // writes the new token's K and V there before any copy of the pipeline starts
@@ -410,7 +423,10 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
     return (page >= 0 && page < C.n_pages) ? page : -1;
   };
   // an out-of-range page id issues no copy (the stage barrier is completed by a
-  // plain arrive) and is recorded; the tile is then skipped
+  // plain arrive) and is recorded; the tile is then skipped.  Diagnostics: with
+  // p.withhold, worker 0 of CTA (0, 0, 0) issues nothing for its tile 0, so its
+  // first wait runs out after the wait bound (a phase that nothing completes)
+  const bool withheld = p.withhold && w == 0 && split == 0 && g == 0 && b == 0;
   auto issue = [&](int u, int page) {
     if (lane == 0) {
       const uint32_t st = ring + (u & 1) * LY.stage_bytes;
@@ -435,7 +451,10 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   };
   // the first two copies go out before the q set-up, whose loads overlap them
   int issued = 0;
-  for (; issued < min(2, n_my); ++issued) issue(issued, page_of(issued));
+  for (; issued < min(2, n_my); ++issued) {
+    const int page = page_of(issued);
+    if (!(withheld && issued == 0)) issue(issued, page);
+  }
 
   // ---- q fragments (B operand of S^T = K q^T): lane holds head r0, dims
   // 64 i + 16 c + 4 j + e of k-step 4 i + j
@@ -709,6 +728,7 @@ __global__ void __launch_bounds__(32 * (QF32 ? kMaxWorkersF32 : kMaxWorkers), 1)
   // for its copies still in flight.  A head with nothing visible writes zeros,
   // so the merge below needs no test.
   if (aborted && lane == 0) {
+    if (withheld) mbar_arrive(full);   // the withheld tile 0: nothing in flight, close its phase
     for (int u = max(0, issued - 2); u < issued; ++u) {
       const uint64_t t0 = global_ns();
       while (!mbar_try_sleep(full + 8 * (u & 1), (u >> 1) & 1, 20000u) && global_ns() - t0 < kWaitDefaultNs) {
@@ -1483,6 +1503,7 @@ DecodeParams params_of(const Launch& L, const CacheView& C, const AttendPlan& pl
   p.v_new = nullptr;
   p.kv_bf16 = 1;
   p.wait_ns = wait_ns ? wait_ns : kWaitDefaultNs;
+  p.withhold = withheld_copy();
   p.page_div = FastDiv(static_cast<uint32_t>(C.P));
   return p;
 }
